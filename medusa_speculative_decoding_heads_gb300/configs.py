@@ -1,0 +1,105 @@
+"""The five synthetic Medusa verify-step workloads, by name and size.
+
+Each workload fixes the shapes of one decoding step: batch ``B``, hidden size
+``d``, vocabulary ``V``, the number of Medusa heads ``K`` with their branching
+factors ``s_1..s_K`` (the candidate tree is the Cartesian product of the
+per-head top-s lists), the attention shape (``Hq`` query heads, ``Hkv`` KV
+heads, head dim ``D``), the committed KV length (fixed or drawn per sequence
+from a range), the element type, the acceptance mode and the temperature.
+
+This module holds sizes only: no arithmetic of the method.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Optional, Tuple
+
+GREEDY = 0
+REJECTION = 1
+
+F32 = 0
+BF16 = 1
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    d: int
+    V: int
+    branching: Tuple[int, ...]
+    Hq: int
+    Hkv: int
+    D: int
+    L_range: Tuple[int, int]          # committed KV length: inclusive [lo, hi]
+    dtype: int                        # F32 or BF16 (weights, KV, Q, O, target logits)
+    modes: Tuple[int, ...]            # acceptance modes the workload runs
+    temperature: float
+    target_sigma: float               # std of the synthetic target logits
+    target_corr: float                # correlation of target logits with head logits
+    compact: bool                     # KV compaction listed for the workload
+    w_sigma: float = 0.02             # std of W_k and of the vocab projections
+    note: str = ""
+
+    @property
+    def K(self) -> int:
+        return len(self.branching)
+
+    @property
+    def N(self) -> int:
+        """Node count of the Cartesian tree: root plus every level."""
+        n, cnt = 1, 1
+        for s in self.branching:
+            cnt *= s
+            n += cnt
+        return n
+
+    @property
+    def s_max(self) -> int:
+        return max(self.branching)
+
+    @property
+    def elt(self) -> int:
+        return 4 if self.dtype == F32 else 2
+
+
+WORKLOADS = {
+    "tiny_fp32": Workload(
+        name="tiny_fp32", B=1, d=256, V=1024, branching=(3, 2, 2), Hq=4, Hkv=4, D=64,
+        L_range=(128, 128), dtype=F32, modes=(GREEDY, REJECTION), temperature=1.0,
+        target_sigma=2.0, target_corr=0.0, compact=False,
+        note="tiny fp32 step, batch 1, 22-node tree, greedy plus rejection sampling at T=1"),
+    "vicuna7b_b1": Workload(
+        name="vicuna7b_b1", B=1, d=4096, V=32000, branching=(4, 3, 2, 1), Hq=32, Hkv=32, D=128,
+        L_range=(2048, 2048), dtype=BF16, modes=(GREEDY,), temperature=0.0,
+        target_sigma=3.0, target_corr=0.0, compact=False,
+        note="Vicuna-7B-shaped step, batch 1, bf16, 65-node tree, greedy"),
+    "vicuna13b_b8": Workload(
+        name="vicuna13b_b8", B=8, d=5120, V=32000, branching=(5, 3, 2, 1, 1), Hq=40, Hkv=40, D=128,
+        L_range=(1024, 4096), dtype=BF16, modes=(REJECTION,), temperature=1.0,
+        target_sigma=3.0, target_corr=0.8, compact=False,
+        note="Vicuna-13B-shaped step, batch 8, bf16, 111-node tree, rejection sampling at T=1"),
+    "vicuna33b_b16": Workload(
+        name="vicuna33b_b16", B=16, d=6656, V=32000, branching=(4, 3, 2, 1), Hq=52, Hkv=52, D=128,
+        L_range=(8192, 8192), dtype=BF16, modes=(GREEDY,), temperature=0.0,
+        target_sigma=3.0, target_corr=0.0, compact=True,
+        note="Vicuna-33B-shaped step, batch 16, bf16, 65-node tree, greedy plus KV compaction"),
+    "gqa7b_b32": Workload(
+        name="gqa7b_b32", B=32, d=4096, V=32000, branching=(4, 3, 2, 1), Hq=32, Hkv=8, D=128,
+        L_range=(4096, 16384), dtype=BF16, modes=(REJECTION,), temperature=0.7,
+        target_sigma=3.0, target_corr=0.8, compact=True,
+        note="7B GQA-shaped step, batch 32, bf16, 65-node tree, rejection sampling at T=0.7 plus KV compaction"),
+}
+
+ORDER = ["tiny_fp32", "vicuna7b_b1", "vicuna13b_b8", "vicuna33b_b16", "gqa7b_b32"]
+
+
+def get(name: str) -> Workload:
+    return WORKLOADS[name]
+
+
+def scaled(w: Workload, **overrides) -> Workload:
+    """A copy of ``w`` with some sizes replaced (small parity cases of a workload)."""
+    fields = {k: getattr(w, k) for k in w.__dataclass_fields__}
+    fields.update(overrides)
+    return Workload(**fields)
