@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""Medusa verify-step throughput on GB300 (steps/s), with the HBM roofline.
+
+One step = the whole hot path on one batch of synthetic input, as five
+library calls on one stream: Medusa heads (residual block, vocab projection,
+top-s) -> candidate tree -> tree attention -> acceptance -> KV compaction.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+N > 1 runs one independent replica per GPU (launched by torch.distributed.run);
+the step has no exchange, so there is no collective on the data path and the
+scaling is weak. `--impl reference` times the CPU oracle (plain float64
+numpy) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from medusa_speculative_decoding_heads_gb300 import configs, synth  # noqa: E402
+from medusa_speculative_decoding_heads_gb300.configs import F32, GREEDY, REJECTION  # noqa: E402
+
+METRIC = "Medusa verify steps/s (heads+tree-attn+accept); HBM GB/s vs 8 TB/s"
+UNIT = "steps/s"
+DEFAULT_WORKLOAD = "vicuna7b_b1"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per launch of the dominant call from the committed ncu capture, by
+# workload; None until a capture of the current kernels exists.
+NCU_TRAFFIC_BYTES = {}
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=configs.ORDER)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def algorithmic_bytes(w, L, acc, mode, with_bias=False):
+    """Minimum bytes one step must move (each term counted once)."""
+    elt = w.elt
+    B, d, V, K, N = w.B, w.d, w.V, w.K, w.N
+    heads = K * (d * d + d * V + (d if with_bias else 0)) * elt + B * d * elt
+    logits = 2 * B * K * V * 4 if mode == REJECTION else 0
+    kv = int(np.sum(L)) * w.Hkv * w.D * 2 * elt
+    tree = B * N * (w.Hq + 2 * w.Hkv) * w.D * elt
+    out = B * N * w.Hq * w.D * elt
+    visited = int(np.sum(np.asarray(acc) + 1)) * V * elt
+    return {"heads": heads, "logits": logits, "kv": kv, "tree_qkv": tree, "attn_out": out, "target_rows": visited,
+            "total": heads + logits + kv + tree + out + visited}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def oracle_inputs_from(si, tl):
+    f = lambda t: t.detach().to("cpu", torch.float32).double().numpy()
+    return {"h": f(si.h), "W": f(si.W), "b": None if si.bias is None else f(si.bias), "U": f(si.U),
+            "Q": f(si.Q), "Kc": f(si.Kc), "Vc": f(si.Vc), "tl": f(tl), "root": si.root_token, "L": si.L,
+            "L_cap": si.L_cap, "u_acc": si.u_acc, "u_res": si.u_res}
+
+
+def oracle_step(O, w, mode, x):
+    r, z = O.medusa_heads(x["h"], x["W"], x["b"], x["U"])
+    topk, _ = O.heads_top_s(z, w.branching)
+    tree = O.tree_build(w.branching, x["root"], topk, x["L"], x["L_cap"])
+    O.tree_attention(x["Q"], x["Kc"], x["Vc"], x["L"], tree["mask"], w.Hq, w.Hkv)
+    ver = O.verify_batch(mode, tree, x["tl"], w.K, head_logits=z, u_acc=x["u_acc"], u_res=x["u_res"],
+                         T=w.temperature)
+    O.kv_compact(x["Kc"], x["Vc"], x["L"], ver["acc"], ver["path"])
+    return ver
+
+
+def time_oracle(w, mode, x, steps, warmup=0, budget_s=None):
+    from oracle import medusa_oracle as O
+    for _ in range(warmup):
+        oracle_step(O, w, mode, x)
+    times = []
+    t_all = time.perf_counter()
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle_step(O, w, mode, x)
+        times.append(time.perf_counter() - t0)
+        if budget_s is not None and time.perf_counter() - t_all > budget_s:
+            break
+    return times
+
+
+def cpu_cores():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = configs.get(args.workload)
+    mode = w.modes[0]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    si = synth.make_step_inputs(w, seed=args.seed, device=dev)
+    tl = make_targets(w, si, dev, mode, args.seed, via_library=False)
+    x = oracle_inputs_from(si, tl)
+    del si, tl
+    if dev == "cuda":
+        torch.cuda.empty_cache()
+    times = time_oracle(w, mode, x, args.steps, warmup=args.warmup)
+    total = sum(times)
+    value = len(times) / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": len(times), "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "B": w.B, "mode": "greedy" if mode == GREEDY else "rejection"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"one full oracle step of {w.name} (B={w.B}) per timed step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def make_targets(w, si, dev, mode, seed, via_library=True):
+    """Target logits: independent, or correlated with this step's head logits."""
+    if w.target_corr == 0.0:
+        return synth.target_logits(w, seed, device=dev)
+    if via_library:
+        # head logits and node depths from the library itself (setup, outside any timed region)
+        from medusa_speculative_decoding_heads_gb300.step import DeviceStep
+        st = DeviceStep(w, REJECTION, si.L_cap, dev)
+        st.heads(si.h, si.W, si.bias, si.U, write_logits=True)
+        st.tree_build(torch.from_numpy(si.root_token).to(dev), torch.from_numpy(si.L).to(dev))
+        zhat, depth = st.logits, st.depth.cpu().numpy()
+    else:
+        # the reference arm: everything from the CPU oracle
+        from oracle import medusa_oracle as O
+        f = lambda t: t.detach().to("cpu", torch.float32).double().numpy()
+        _, z = O.medusa_heads(f(si.h), f(si.W), None if si.bias is None else f(si.bias), f(si.U))
+        zhat, depth = torch.from_numpy(z).float(), O.tree_layout(w.branching)["depth"]
+    return synth.target_logits(w, seed, device=dev, zhat=zhat, depth=depth)
+
+
+def run_ours(args):
+    from medusa_speculative_decoding_heads_gb300 import _build, binding as mb
+    from medusa_speculative_decoding_heads_gb300.step import DeviceStep, to_device_inputs
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+    mb.load()
+
+    w = configs.get(args.workload)
+    mode = w.modes[0]
+    seed = args.seed + 1000 * rank
+    si = synth.make_step_inputs(w, seed=seed, device=dev)
+    tl = make_targets(w, si, dev, mode, seed)
+    inp = to_device_inputs(si, tl, dev)
+    L0 = inp.L.clone()
+    stream = torch.cuda.current_stream(dev)
+    st = DeviceStep(w, mode, si.L_cap, dev)
+    write_logits = mode == REJECTION
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    calls = [
+        lambda: st.heads(inp.h, inp.W, inp.bias, inp.U, write_logits=write_logits),
+        lambda: st.tree_build(inp.root_token, inp.L),
+        lambda: st.tree_attention(inp.Q, inp.Kc, inp.Vc, inp.L),
+        lambda: st.verify(inp.target_logits, inp.u_acc, inp.u_res),
+        lambda: st.kv_compact(inp.Kc, inp.Vc, inp.L),
+    ]
+    names = ["heads", "tree_build", "tree_attention", "verify", "kv_compact"]
+
+    def one_step(marks=None):
+        inp.L.copy_(L0, non_blocking=True)
+        for i, call in enumerate(calls):
+            if marks is not None:
+                marks[i].record(stream)
+            call()
+        if marks is not None:
+            marks[len(calls)].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        one_step()
+    torch.cuda.synchronize()
+    acc = st.acc.cpu().numpy()
+
+    marks = [[ev() for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    t0, t1 = ev(), ev()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    n0 = mb.launch_count()
+    t0.record(stream)
+    for k in range(args.steps):
+        one_step(marks[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    launches = mb.launch_count() - n0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed_ms = t0.elapsed_time(t1)
+    per_call = {n: statistics.mean(m[i].elapsed_time(m[i + 1]) for m in marks) for i, n in enumerate(names)}
+    heads_ms = per_call["heads"]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = world * args.steps / (elapsed_ms / 1000.0)
+
+    e2e = None if args.no_e2e else run_e2e(w, st, inp, L0, tl, si, args, stream, world)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    hbm, peak_kind = peaks()
+    by = algorithmic_bytes(w, si.L, acc, mode, with_bias=si.bias is not None)
+    heads_bytes = by["heads"] + (w.B * w.K * w.V * 4 if write_logits else 0)
+    achieved = heads_bytes / (heads_ms * 1e-3) / 1e9
+    traffic = NCU_TRAFFIC_BYTES.get(w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32" if w.dtype == F32 else "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "d": w.d, "V": w.V, "K": w.K, "branching": list(w.branching),
+                   "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "L": [int(x) for x in si.L][:4],
+                   "L_sum": int(np.sum(si.L)), "mode": "greedy" if mode == GREEDY else "rejection",
+                   "temperature": w.temperature if mode == REJECTION else None,
+                   "l2": f"inputs larger than L2 ({by['total'] / 1e9:.2f} GB algorithmic per step)",
+                   "parallelism": f"replicas x{world}"},
+        "clocks": clocks,
+        "gpu_launches": launches,
+        "roofline": {"bound": "hbm", "kernel": "medusa_heads (residual + vocab projection GEMV, top-s)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": traffic, "peak_source": f"hbm_gbs of {peak_kind}",
+                     "algorithmic_bytes": heads_bytes, "avg_launch_ms": heads_ms},
+        "step_roofline": {"algorithmic_bytes": by["total"], "achieved_gbs": by["total"] / (ms_per_step * 1e-3) / 1e9,
+                          "frac": by["total"] / (ms_per_step * 1e-3) / 1e9 / hbm, "bytes_by_term": by},
+        "breakdown_ms": dict(per_call, step=ms_per_step),
+        "accepted_per_step": float(np.mean(acc + 1)),
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, mode, si, tl)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_e2e(w, st, inp, L0, tl, si, args, stream, world):
+    """The same step with per-step inputs copied from pinned host memory and results read back."""
+    N = w.N
+    host = {
+        "h": inp.h.cpu().pin_memory(), "Q": inp.Q.cpu().pin_memory(), "tl": inp.target_logits.cpu().pin_memory(),
+        "u_acc": inp.u_acc.cpu().pin_memory(), "u_res": inp.u_res.cpu().pin_memory(),
+        "root": inp.root_token.cpu().pin_memory(), "L": L0.cpu().pin_memory(),
+    }
+    Lh = [int(x) for x in si.L]
+    tk = torch.stack([inp.Kc[b, :, Lh[b]:Lh[b] + N].cpu() for b in range(w.B)]).pin_memory()
+    tv = torch.stack([inp.Vc[b, :, Lh[b]:Lh[b] + N].cpu() for b in range(w.B)]).pin_memory()
+    out_tok = torch.empty_like(st.out_tokens, device="cpu").pin_memory()
+    out_n = torch.empty_like(st.n_out, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + 2 * tk.numel() * tk.element_size()
+    d2h = out_tok.numel() * 4 + out_n.numel() * 4
+
+    def e2e_step():
+        inp.h.copy_(host["h"], non_blocking=True)
+        inp.Q.copy_(host["Q"], non_blocking=True)
+        inp.target_logits.copy_(host["tl"], non_blocking=True)
+        inp.u_acc.copy_(host["u_acc"], non_blocking=True)
+        inp.u_res.copy_(host["u_res"], non_blocking=True)
+        inp.root_token.copy_(host["root"], non_blocking=True)
+        inp.L.copy_(host["L"], non_blocking=True)
+        for b in range(w.B):
+            inp.Kc[b, :, Lh[b]:Lh[b] + N].copy_(tk[b], non_blocking=True)
+            inp.Vc[b, :, Lh[b]:Lh[b] + N].copy_(tv[b], non_blocking=True)
+        st.run(inp, write_logits=st.mode == REJECTION, compact=True)
+        out_tok.copy_(st.out_tokens, non_blocking=True)
+        out_n.copy_(st.n_out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    steps = max(5, args.steps // 2)
+    if world > 1:
+        torch.distributed.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    if world > 1:
+        t = torch.tensor([ms], device=inp.h.device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": world * steps / (ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+def cpu_baseline(w, mode, si, tl):
+    x = oracle_inputs_from(si, tl)
+    times = time_oracle(w, mode, x, steps=50, warmup=1, budget_s=15.0)
+    return {"value": len(times) / sum(times), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{len(times)} full oracle steps of {w.name} (B={w.B}), float64 numpy, inputs pre-decoded"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

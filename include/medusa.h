@@ -1,0 +1,186 @@
+/*
+ * medusa.h — C ABI of libmedusa: one Medusa speculative-decoding verify step on
+ * one GB300 GPU (sm_103a).
+ *
+ * The step, as the source pages describe it:
+ *   1. K Medusa heads on the backbone's last hidden state h: a residual block
+ *      r_k = h + SiLU(W_k h + b_k) and a vocab projection z_k = U_k r_k, then a
+ *      top-s_k list per head  ["Medusa 심층 아키텍처" (techknowgenie), section
+ *      "Medusa의 핵심 철학", equations h_t^(k) and p_k; section "소스코드 레벨 구조
+ *      분석", MedusaHead and generate_candidates].
+ *   2. The Cartesian candidate tree, its ancestor mask and position ids
+ *      [same page, section "트리 어텐션", tree-topology example and the TreeMask
+ *      equation].
+ *   3. Tree attention: every node attends to the committed KV cache plus its own
+ *      ancestors, all nodes in one pass [same page, section "트리 어텐션"].
+ *   4. Acceptance — greedy longest matching path with a bonus token ["최적화 2편"
+ *      (beengineer500), section 1.3] or rejection sampling with r = min(1, p/q)
+ *      and residual max(0, p - q)/sum ["Medusa 심층 아키텍처", section "수학적
+ *      무손실 보장", equations alpha(x) and p'(x); "Speculative Decoding 원리와
+ *      가속 아키텍처" (blog.huny.dev), section 2.1] — then compaction of the
+ *      accepted path's KV rows [blog.huny.dev, section 5 Case 2 and section 6].
+ *
+ * Conventions (every entry point):
+ *   - Pointers are DEVICE pointers unless a parameter says otherwise; the caller
+ *     owns every buffer. The library never allocates or frees device memory;
+ *     scratch comes from a caller-provided workspace of medusa_workspace_size()
+ *     bytes (256-byte aligned).
+ *   - Calls only enqueue work on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and never synchronize.
+ *   - Return MEDUSA_OK (0) or a negative MEDUSA_ERR_*; on error nothing is
+ *     enqueued. Device-side data errors never trap: they set bits in a
+ *     per-sequence `flags` word and the affected sequence is skipped.
+ *   - Layouts are dense row-major with the shapes given; "elt" is float when
+ *     cfg->dtype == MEDUSA_F32 and bf16 (uint16 bit pattern) when MEDUSA_BF16.
+ *   - N = 1 + sum_{k=1..K} prod_{j<=k} s_j is the node count (N <= 128),
+ *     s_max = max_k s_k (<= 8), K <= 8.
+ *   - Tree node order: breadth first; within a depth, lexicographic in the
+ *     path of sibling ranks (first rank most significant). Node 0 is the root,
+ *     which is the already committed next token of each sequence.
+ */
+#ifndef MEDUSA_H_
+#define MEDUSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MEDUSA_API __attribute__((visibility("default")))
+#else
+#define MEDUSA_API
+#endif
+
+typedef struct CUstream_st* medusa_stream_t; /* same type as cudaStream_t */
+
+enum { MEDUSA_F32 = 0, MEDUSA_BF16 = 1 };
+enum { MEDUSA_GREEDY = 0, MEDUSA_REJECTION = 1 };
+
+enum {
+  MEDUSA_OK = 0,
+  MEDUSA_ERR_INVALID_ARG = -1, /* null pointer, non-positive size, bad enum   */
+  MEDUSA_ERR_UNSUPPORTED = -2, /* valid but outside the built limits          */
+  MEDUSA_ERR_CAPACITY = -3,    /* host-visible capacity violation              */
+  MEDUSA_ERR_CUDA = -4,        /* a CUDA launch or attribute call failed       */
+  MEDUSA_ERR_TIMEOUT = -5      /* reserved: a bounded device-side wait expired */
+};
+
+/* Per-sequence flag bits (uint32). */
+#define MEDUSA_FLAG_RS_NEAR_TIE 1u  /* some acceptance test had |u - r| < 1e-6            */
+#define MEDUSA_FLAG_CDF_NEAR_TIE 2u /* an inverse-CDF draw fell within 1e-6*total of a step */
+#define MEDUSA_FLAG_CAPACITY 4u     /* L_b < 0 or L_b + N > L_cap: sequence skipped      */
+
+typedef struct {
+  int32_t B;            /* sequences in the step                                 */
+  int32_t d;            /* hidden size                                           */
+  int32_t V;            /* vocabulary size                                       */
+  int32_t K;            /* Medusa heads = tree depth (1..8)                      */
+  int32_t branching[8]; /* s_1..s_K: candidates kept per head (1..8)             */
+  int32_t Hq;           /* query heads                                           */
+  int32_t Hkv;          /* KV heads (Hq % Hkv == 0)                              */
+  int32_t D;            /* head dim (64 or 128)                                  */
+  int32_t L_cap;        /* KV cache rows per (sequence, KV head)                 */
+  int32_t dtype;        /* MEDUSA_F32 or MEDUSA_BF16                             */
+  int32_t mode;         /* MEDUSA_GREEDY or MEDUSA_REJECTION                     */
+  float temperature;    /* T > 0 for MEDUSA_REJECTION (logits are divided by T)  */
+} medusa_cfg;
+
+/* Node count N of the configured tree. Host only; `N` is a host pointer. */
+MEDUSA_API int medusa_node_count(const medusa_cfg* cfg, int32_t* N);
+
+/* Workspace bytes needed by medusa_heads and medusa_tree_attention for this
+ * configuration (one workspace may serve both, since they use disjoint parts).
+ * Host only; `bytes` is a host pointer. */
+MEDUSA_API int medusa_workspace_size(const medusa_cfg* cfg, size_t* bytes);
+
+/* Step 1 — Medusa heads and per-head top-s.
+ *   h      [B][d] elt          backbone last hidden state
+ *   W      [K][d][d] elt       W[k][o][i]: residual-layer weight, input i -> output o
+ *   bias   [K][d] elt          b_k, may be NULL (zero bias)
+ *   U      [K][V][d] elt       U[k][v][i]: vocab projection of head k
+ *   logits [B][K][V] float     z_k per sequence; may be NULL in MEDUSA_GREEDY mode
+ *                              (then kept in the workspace). Needed as
+ *                              `head_logits` by medusa_verify in MEDUSA_REJECTION.
+ *   topk   [B][K][s_max] int32 indices of the s_k largest z_k entries, descending,
+ *                              ties to the lower index; -1 beyond s_k.
+ * r_k is kept in float32; accumulation is float32. */
+MEDUSA_API int medusa_heads(const medusa_cfg* cfg, const void* h, const void* W, const void* bias,
+                 const void* U, float* logits, int32_t* topk, void* workspace,
+                 medusa_stream_t stream);
+
+/* Step 2 — Cartesian candidate tree.
+ *   root_token [B] int32, topk [B][K][s_max] int32, L [B] int32 (committed lengths).
+ * Outputs (the first five are identical for every sequence):
+ *   parent [N] int32 (-1 at the root), depth [N] int32, first_child [N] int32
+ *   (-1 at depth K; children of a node are contiguous, in rank order),
+ *   mask [N][N] uint8 (1 iff column is an ancestor of the row or the row itself),
+ *   anc_bits [N][2] uint64 (bit j of word j/64 = mask[i][j]),
+ *   tokens [B][N] int32 (root_token, then topk[b][depth-1][rank]),
+ *   pos [B][N] int32 (L_b + depth),
+ *   flags [B] uint32 (may be NULL): OVERWRITTEN with MEDUSA_FLAG_CAPACITY or 0. */
+MEDUSA_API int medusa_tree_build(const medusa_cfg* cfg, const int32_t* root_token, const int32_t* topk,
+                      const int32_t* L, int32_t* parent, int32_t* depth, int32_t* first_child,
+                      uint8_t* mask, uint64_t* anc_bits, int32_t* tokens, int32_t* pos,
+                      uint32_t* flags, medusa_stream_t stream);
+
+/* Step 3 — tree attention.
+ *   Q  [B][N][Hq][D] elt          queries of the tree nodes
+ *   Kc [B][Hkv][L_cap][D] elt     keys: committed rows [0, L_b), tree rows L_b + j
+ *   Vc [B][Hkv][L_cap][D] elt     values, same layout
+ *   L  [B] int32, anc_bits [N][2] uint64 (from medusa_tree_build)
+ *   O  [B][N][Hq][D] elt          softmax(q.k / sqrt(D)) v over the committed rows
+ *                                 and the node's ancestors-or-self; KV head of
+ *                                 query head h is h / (Hq / Hkv).
+ * Softmax and accumulation in float32. A sequence with L_b < 0 or
+ * L_b + N > L_cap gets O = 0. */
+MEDUSA_API int medusa_tree_attention(const medusa_cfg* cfg, const void* Q, const void* Kc, const void* Vc,
+                          const int32_t* L, const uint64_t* anc_bits, void* O, void* workspace,
+                          medusa_stream_t stream);
+
+/* Step 4 — acceptance walk (cfg->mode).
+ *   tokens [B][N], parent [N], first_child [N] int32 (from medusa_tree_build)
+ *   target_logits [B][N][V] elt   target model logits at every tree node
+ *   head_logits [B][K][V] float   z from medusa_heads (MEDUSA_REJECTION only, else NULL)
+ *   u_acc [B][K][s_max] float     acceptance uniforms (REJECTION only, else NULL)
+ *   u_res [B][K+1] float          resampling uniforms (REJECTION only, else NULL)
+ * Outputs: acc [B] accepted drafts; path [B][K+1] node ids (path[0] = 0, -1 pad);
+ *   out_tokens [B][K+1] the accepted tokens then the bonus/correction token
+ *   (-1 pad); n_out [B] = acc + 1; flags [B] uint32: this call ORs in its
+ *   MEDUSA_FLAG_* bits (clear or initialise it first, e.g. with medusa_tree_build).
+ * GREEDY: the child whose token equals argmax(target_logits[node]) (ties to
+ * the lowest id) is accepted until none matches; the bonus is that argmax at
+ * the last accepted node.
+ * REJECTION: at the current node, p = softmax(target/T), q = softmax(z_depth/T);
+ * children in rank order are accepted when u < min(1, p(x)/q(x)), each
+ * rejection replacing p by max(0, p - q)/sum; when all are rejected the bonus
+ * is the smallest y with cdf_p(y) > u_res * sum(p); after an accepted leaf it is
+ * drawn from softmax(target[leaf]/T). Requires V <= 32768. */
+MEDUSA_API int medusa_verify(const medusa_cfg* cfg, const int32_t* tokens, const int32_t* parent,
+                  const int32_t* first_child, const void* target_logits, const float* head_logits,
+                  const float* u_acc, const float* u_res, int32_t* acc, int32_t* path,
+                  int32_t* out_tokens, int32_t* n_out, uint32_t* flags, medusa_stream_t stream);
+
+/* Step 5 — KV compaction of the accepted path, in place.
+ *   Kc, Vc [B][Hkv][L_cap][D] elt: for r = 0..acc_b, row L_b + r <- row L_b + path[b][r]
+ *   in every KV head (sources are read before they can be overwritten).
+ *   L [B] int32 in/out: L_b += acc_b + 1.
+ *   kv_map [B][K+1] int32: source node per destination slot, -1 pad.
+ * Sequences with L_b < 0 or L_b + N > L_cap are left unchanged (kv_map = -1). */
+MEDUSA_API int medusa_kv_compact(const medusa_cfg* cfg, void* Kc, void* Vc, int32_t* L, const int32_t* acc,
+                      const int32_t* path, int32_t* kv_map, medusa_stream_t stream);
+
+/* Number of kernels this library has enqueued in this process so far (host-side
+ * counter, for diagnostics; no counterpart on the pages). */
+MEDUSA_API uint64_t medusa_launch_count(void);
+
+/* Human-readable text of a status code (static storage). */
+MEDUSA_API const char* medusa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEDUSA_H_ */

@@ -1,0 +1,161 @@
+"""Thin Python binding of libmedusa (ctypes): argument marshalling only.
+
+Every function takes the same arguments as the C entry point of the same name
+in include/medusa.h. Tensors are passed as raw device pointers (``data_ptr``);
+``None`` becomes a null pointer. A non-zero status raises ``MedusaError``. No
+computation happens here and there is no fallback: if the library cannot be
+loaded, ``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmedusa.so")
+
+F32, BF16 = 0, 1
+GREEDY, REJECTION = 0, 1
+FLAG_RS_NEAR_TIE, FLAG_CDF_NEAR_TIE, FLAG_CAPACITY = 1, 2, 4
+
+ENTRY_POINTS = ("medusa_node_count", "medusa_workspace_size", "medusa_heads", "medusa_tree_build",
+                "medusa_tree_attention", "medusa_verify", "medusa_kv_compact", "medusa_launch_count",
+                "medusa_status_string")
+
+
+class MedusaError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn} failed: {status} ({text})")
+        self.status = status
+
+
+class Cfg(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("d", ctypes.c_int32), ("V", ctypes.c_int32), ("K", ctypes.c_int32),
+                ("branching", ctypes.c_int32 * 8), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("L_cap", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("mode", ctypes.c_int32), ("temperature", ctypes.c_float)]
+
+
+def make_cfg(B: int, d: int, V: int, branching: Sequence[int], Hq: int, Hkv: int, D: int, L_cap: int,
+             dtype: int, mode: int, temperature: float = 1.0) -> Cfg:
+    c = Cfg()
+    c.B, c.d, c.V, c.K = B, d, V, len(branching)
+    for i, s in enumerate(branching):
+        c.branching[i] = int(s)
+    c.Hq, c.Hkv, c.D, c.L_cap = Hq, Hkv, D, L_cap
+    c.dtype, c.mode, c.temperature = dtype, mode, float(temperature)
+    return c
+
+
+_lib: Optional[ctypes.CDLL] = None
+P = ctypes.c_void_p
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmedusa.so (build it first with ``_build.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libmedusa not built: {path} is missing (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    cp = ctypes.POINTER(Cfg)
+    sig = {
+        "medusa_node_count": [cp, ctypes.POINTER(ctypes.c_int32)],
+        "medusa_workspace_size": [cp, ctypes.POINTER(ctypes.c_size_t)],
+        "medusa_heads": [cp, P, P, P, P, P, P, P, P],
+        "medusa_tree_build": [cp, P, P, P, P, P, P, P, P, P, P, P, P],
+        "medusa_tree_attention": [cp, P, P, P, P, P, P, P, P],
+        "medusa_verify": [cp, P, P, P, P, P, P, P, P, P, P, P, P, P],
+        "medusa_kv_compact": [cp, P, P, P, P, P, P, P],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    lib.medusa_launch_count.argtypes = []
+    lib.medusa_launch_count.restype = ctypes.c_uint64
+    lib.medusa_status_string.argtypes = [ctypes.c_int]
+    lib.medusa_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(name: str, status: int) -> None:
+    if status != 0:
+        raise MedusaError(name, status, load().medusa_status_string(status).decode())
+
+
+def status_string(status: int) -> str:
+    return load().medusa_status_string(status).decode()
+
+
+def launch_count() -> int:
+    """Kernels libmedusa has enqueued in this process so far."""
+    return int(load().medusa_launch_count())
+
+
+def node_count(cfg: Cfg) -> int:
+    n = ctypes.c_int32()
+    _check("medusa_node_count", load().medusa_node_count(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def workspace_size(cfg: Cfg) -> int:
+    n = ctypes.c_size_t()
+    _check("medusa_workspace_size", load().medusa_workspace_size(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def heads(cfg, h, W, bias, U, logits, topk, workspace, stream=None):
+    _check("medusa_heads", load().medusa_heads(ctypes.byref(cfg), _ptr(h), _ptr(W), _ptr(bias), _ptr(U),
+                                                 _ptr(logits), _ptr(topk), _ptr(workspace), _stream(stream)))
+
+
+def tree_build(cfg, root_token, topk, L, parent, depth, first_child, mask, anc_bits, tokens, pos, flags,
+               stream=None):
+    _check("medusa_tree_build", load().medusa_tree_build(
+        ctypes.byref(cfg), _ptr(root_token), _ptr(topk), _ptr(L), _ptr(parent), _ptr(depth), _ptr(first_child),
+        _ptr(mask), _ptr(anc_bits), _ptr(tokens), _ptr(pos), _ptr(flags), _stream(stream)))
+
+
+def tree_attention(cfg, Q, Kc, Vc, L, anc_bits, O, workspace, stream=None):
+    _check("medusa_tree_attention", load().medusa_tree_attention(
+        ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), _ptr(L), _ptr(anc_bits), _ptr(O), _ptr(workspace),
+        _stream(stream)))
+
+
+def verify(cfg, tokens, parent, first_child, target_logits, head_logits, u_acc, u_res, acc, path, out_tokens,
+           n_out, flags, stream=None):
+    _check("medusa_verify", load().medusa_verify(
+        ctypes.byref(cfg), _ptr(tokens), _ptr(parent), _ptr(first_child), _ptr(target_logits), _ptr(head_logits),
+        _ptr(u_acc), _ptr(u_res), _ptr(acc), _ptr(path), _ptr(out_tokens), _ptr(n_out), _ptr(flags),
+        _stream(stream)))
+
+
+def kv_compact(cfg, Kc, Vc, L, acc, path, kv_map, stream=None):
+    _check("medusa_kv_compact", load().medusa_kv_compact(
+        ctypes.byref(cfg), _ptr(Kc), _ptr(Vc), _ptr(L), _ptr(acc), _ptr(path), _ptr(kv_map), _stream(stream)))
+
+
+def raw_call(name: str, *args) -> int:
+    """Call an entry point with already-marshalled arguments; returns the status."""
+    return getattr(load(), name)(*args)

@@ -1,0 +1,143 @@
+// C ABI entry points of libmedusa: argument checks, then kernel launches.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "common.cuh"
+
+namespace medusa {
+
+static std::atomic<unsigned long long> g_launches{0};
+void note_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by every call: sizes, enums and the built limits.
+int check_cfg(const medusa_cfg* c) {
+  if (!c) return MEDUSA_ERR_INVALID_ARG;
+  if (c->B < 1 || c->d < 1 || c->V < 1 || c->K < 1 || c->Hq < 1 || c->Hkv < 1 || c->D < 1 || c->L_cap < 1)
+    return MEDUSA_ERR_INVALID_ARG;
+  if (c->dtype != MEDUSA_F32 && c->dtype != MEDUSA_BF16) return MEDUSA_ERR_INVALID_ARG;
+  if (c->mode != MEDUSA_GREEDY && c->mode != MEDUSA_REJECTION) return MEDUSA_ERR_INVALID_ARG;
+  if (c->K > kMaxK) return MEDUSA_ERR_UNSUPPORTED;
+  for (int k = 0; k < c->K; ++k) {
+    if (c->branching[k] < 1) return MEDUSA_ERR_INVALID_ARG;
+    if (c->branching[k] > kMaxS || c->branching[k] > c->V) return MEDUSA_ERR_UNSUPPORTED;
+  }
+  long n = 1, cnt = 1;
+  for (int k = 0; k < c->K; ++k) {
+    cnt *= c->branching[k];
+    n += cnt;
+    if (n > kMaxN) return MEDUSA_ERR_UNSUPPORTED;
+  }
+  if (c->Hq % c->Hkv != 0) return MEDUSA_ERR_UNSUPPORTED;
+  if (c->D != 64 && c->D != 128) return MEDUSA_ERR_UNSUPPORTED;
+  if (c->L_cap < n) return MEDUSA_ERR_CAPACITY;
+  if (c->mode == MEDUSA_REJECTION && !(c->temperature > 0.f)) return MEDUSA_ERR_INVALID_ARG;
+  return MEDUSA_OK;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? MEDUSA_OK : MEDUSA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace medusa
+
+using namespace medusa;
+
+extern "C" {
+
+int medusa_node_count(const medusa_cfg* cfg, int32_t* N) {
+  int s = check_cfg(cfg);
+  if (s != MEDUSA_OK && s != MEDUSA_ERR_CAPACITY) return s;
+  if (!N) return MEDUSA_ERR_INVALID_ARG;
+  *N = tree_shape(*cfg).N;
+  return MEDUSA_OK;
+}
+
+int medusa_workspace_size(const medusa_cfg* cfg, size_t* bytes) {
+  int s = check_cfg(cfg);
+  if (s != MEDUSA_OK) return s;
+  if (!bytes) return MEDUSA_ERR_INVALID_ARG;
+  *bytes = align_up(heads_workspace(*cfg), 256) + align_up(attention_workspace(*cfg), 256);
+  return MEDUSA_OK;
+}
+
+int medusa_heads(const medusa_cfg* cfg, const void* h, const void* W, const void* bias, const void* U, float* logits,
+                 int32_t* topk, void* workspace, medusa_stream_t stream) {
+  int s = check_cfg(cfg);
+  if (s != MEDUSA_OK) return s;
+  if (!h || !W || !U || !topk || !workspace) return MEDUSA_ERR_INVALID_ARG;
+  if (!logits && cfg->mode == MEDUSA_REJECTION) return MEDUSA_ERR_INVALID_ARG;
+  if (cfg->dtype == MEDUSA_BF16) {
+    if (cfg->d % 64 != 0) return MEDUSA_ERR_UNSUPPORTED;
+    if (!aligned16(h) || !aligned16(W) || !aligned16(U)) return MEDUSA_ERR_INVALID_ARG;
+  }
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MEDUSA_ERR_INVALID_ARG;
+  return from_cuda(launch_heads(*cfg, h, W, bias, U, logits, topk, workspace, (cudaStream_t)stream));
+}
+
+int medusa_tree_build(const medusa_cfg* cfg, const int32_t* root_token, const int32_t* topk, const int32_t* L,
+                      int32_t* parent, int32_t* depth, int32_t* first_child, uint8_t* mask, uint64_t* anc_bits,
+                      int32_t* tokens, int32_t* pos, uint32_t* flags, medusa_stream_t stream) {
+  int s = check_cfg(cfg);
+  if (s != MEDUSA_OK) return s;
+  if (!root_token || !topk || !L || !parent || !depth || !first_child || !mask || !anc_bits || !tokens || !pos)
+    return MEDUSA_ERR_INVALID_ARG;
+  return from_cuda(launch_tree_build(*cfg, root_token, topk, L, parent, depth, first_child, mask, anc_bits, tokens,
+                                     pos, flags, (cudaStream_t)stream));
+}
+
+int medusa_tree_attention(const medusa_cfg* cfg, const void* Q, const void* Kc, const void* Vc, const int32_t* L,
+                          const uint64_t* anc_bits, void* O, void* workspace, medusa_stream_t stream) {
+  int s = check_cfg(cfg);
+  if (s != MEDUSA_OK) return s;
+  if (!Q || !Kc || !Vc || !L || !anc_bits || !O || !workspace) return MEDUSA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(Kc) || !aligned16(Vc) || !aligned16(O)) return MEDUSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MEDUSA_ERR_INVALID_ARG;
+  char* ws = static_cast<char*>(workspace) + align_up(heads_workspace(*cfg), 256);
+  return from_cuda(launch_attention(*cfg, Q, Kc, Vc, L, anc_bits, O, ws, (cudaStream_t)stream));
+}
+
+int medusa_verify(const medusa_cfg* cfg, const int32_t* tokens, const int32_t* parent, const int32_t* first_child,
+                  const void* target_logits, const float* head_logits, const float* u_acc, const float* u_res,
+                  int32_t* acc, int32_t* path, int32_t* out_tokens, int32_t* n_out, uint32_t* flags,
+                  medusa_stream_t stream) {
+  int s = check_cfg(cfg);
+  if (s != MEDUSA_OK) return s;
+  if (!tokens || !first_child || !target_logits || !acc || !path || !out_tokens || !n_out || !flags)
+    return MEDUSA_ERR_INVALID_ARG;
+  if (cfg->mode == MEDUSA_REJECTION) {
+    if (!head_logits || !u_acc || !u_res) return MEDUSA_ERR_INVALID_ARG;
+    if (cfg->V > 32768) return MEDUSA_ERR_UNSUPPORTED;
+  }
+  return from_cuda(launch_verify(*cfg, tokens, parent, first_child, target_logits, head_logits, u_acc, u_res, acc,
+                                 path, out_tokens, n_out, flags, (cudaStream_t)stream));
+}
+
+int medusa_kv_compact(const medusa_cfg* cfg, void* Kc, void* Vc, int32_t* L, const int32_t* acc, const int32_t* path,
+                      int32_t* kv_map, medusa_stream_t stream) {
+  int s = check_cfg(cfg);
+  if (s != MEDUSA_OK) return s;
+  if (!Kc || !Vc || !L || !acc || !path || !kv_map) return MEDUSA_ERR_INVALID_ARG;
+  if (!aligned16(Kc) || !aligned16(Vc)) return MEDUSA_ERR_INVALID_ARG;
+  return from_cuda(launch_kv_compact(*cfg, Kc, Vc, L, acc, path, kv_map, (cudaStream_t)stream));
+}
+
+uint64_t medusa_launch_count(void) { return (uint64_t)g_launches.load(std::memory_order_relaxed); }
+
+const char* medusa_status_string(int status) {
+  switch (status) {
+    case MEDUSA_OK: return "ok";
+    case MEDUSA_ERR_INVALID_ARG: return "invalid argument";
+    case MEDUSA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MEDUSA_ERR_CAPACITY: return "KV cache capacity exceeded";
+    case MEDUSA_ERR_CUDA: return "CUDA launch error";
+    case MEDUSA_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,105 @@
+// Shared device/host helpers of libmedusa (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/medusa.h"
+
+namespace medusa {
+
+constexpr int kMaxK = 8;
+constexpr int kMaxS = 8;
+constexpr int kMaxN = 128;
+
+// Tree shape derived from the configuration: level counts and offsets.
+struct TreeShape {
+  int K;
+  int N;
+  int s_max;
+  int s[kMaxK + 1];     // s[1..K]
+  int cnt[kMaxK + 1];   // cnt[d] = prod_{j<=d} s_j, cnt[0] = 1
+  int off[kMaxK + 2];   // off[d] = sum_{e<d} cnt[e]; off[K+1] = N
+};
+
+inline TreeShape tree_shape(const medusa_cfg& c) {
+  TreeShape t{};
+  t.K = c.K;
+  t.cnt[0] = 1;
+  t.off[0] = 0;
+  t.s_max = 0;
+  for (int d = 1; d <= c.K; ++d) {
+    t.s[d] = c.branching[d - 1];
+    t.cnt[d] = t.cnt[d - 1] * t.s[d];
+    t.s_max = t.s[d] > t.s_max ? t.s[d] : t.s_max;
+  }
+  for (int d = 1; d <= c.K + 1; ++d) t.off[d] = t.off[d - 1] + t.cnt[d - 1];
+  t.N = t.off[c.K + 1];
+  return t;
+}
+
+// bf16 <-> f32 as bit patterns (bf16 is the top half of an IEEE f32).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t v) { return __uint_as_float(uint32_t(v) << 16); }
+
+// Round-to-nearest-even f32 -> bf16 bit pattern (inputs here are finite).
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  uint32_t u = __float_as_uint(f);
+  uint32_t r = 0x7fffu + ((u >> 16) & 1u);
+  return uint16_t((u + r) >> 16);
+}
+
+template <typename T> struct Elt;
+template <> struct Elt<float> {
+  __device__ __forceinline__ static float load(const float* p, size_t i) { return p[i]; }
+  __device__ __forceinline__ static void store(float* p, size_t i, float v) { p[i] = v; }
+};
+template <> struct Elt<uint16_t> {
+  __device__ __forceinline__ static float load(const uint16_t* p, size_t i) { return bf16_to_f32(p[i]); }
+  __device__ __forceinline__ static void store(uint16_t* p, size_t i, float v) { p[i] = f32_to_bf16(v); }
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Launchers (each returns a cudaError_t from the launch).
+cudaError_t launch_heads(const medusa_cfg& c, const void* h, const void* W, const void* bias,
+                         const void* U, float* logits, int32_t* topk, void* ws, cudaStream_t st);
+size_t heads_workspace(const medusa_cfg& c);
+
+cudaError_t launch_tree_build(const medusa_cfg& c, const int32_t* root, const int32_t* topk,
+                              const int32_t* L, int32_t* parent, int32_t* depth, int32_t* first_child,
+                              uint8_t* mask, uint64_t* bits, int32_t* tokens, int32_t* pos,
+                              uint32_t* flags, cudaStream_t st);
+
+cudaError_t launch_attention(const medusa_cfg& c, const void* Q, const void* Kc, const void* Vc,
+                             const int32_t* L, const uint64_t* bits, void* O, void* ws, cudaStream_t st);
+size_t attention_workspace(const medusa_cfg& c);
+int attention_mma_warps(int NG, int* row_blocks);
+cudaError_t launch_attention_mma(const medusa_cfg& c, int nsplit, int chunk, const void* Q, const void* Kc,
+                                 const void* Vc, const int32_t* L, const uint64_t* bits, float* o_part, float* ml_part,
+                                 cudaStream_t st);
+
+cudaError_t launch_verify(const medusa_cfg& c, const int32_t* tokens, const int32_t* parent,
+                          const int32_t* first_child, const void* tl, const float* hl,
+                          const float* u_acc, const float* u_res, int32_t* acc, int32_t* path,
+                          int32_t* out_tokens, int32_t* n_out, uint32_t* flags, cudaStream_t st);
+
+cudaError_t launch_kv_compact(const medusa_cfg& c, void* Kc, void* Vc, int32_t* L, const int32_t* acc,
+                              const int32_t* path, int32_t* kv_map, cudaStream_t st);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Host-side count of kernels this library has enqueued (diagnostics).
+void note_launches(int n);
+
+}  // namespace medusa

@@ -1,0 +1,78 @@
+// Cartesian candidate tree: layout, ancestor mask, tokens and position ids.
+//
+// "Medusa 심층 아키텍처" (techknowgenie), section "트리 어텐션": each head keeps its
+// top-s candidates and the candidates of consecutive heads are combined into a
+// tree (the page's example: top-2 x top-3 x top-2); the TreeMask equation makes
+// node i see node j iff j is an ancestor of i or j = i.
+//
+// Node order: breadth first, lexicographic in the sibling-rank path. With
+// cnt_d = prod_{j<=d} s_j and off_d = sum_{e<d} cnt_e, the node at depth d and
+// level index t has parent off_{d-1} + t / s_d, rank t % s_d and first child
+// off_{d+1} + t * s_{d+1}; its token is head d's candidate of that rank.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace medusa {
+namespace {
+
+__device__ __forceinline__ int node_depth(const TreeShape& ts, int n) {
+  int d = 0;
+  while (d < ts.K && n >= ts.off[d + 1]) ++d;
+  return d;
+}
+
+__device__ __forceinline__ int node_parent(const TreeShape& ts, int n) {
+  if (n == 0) return -1;
+  int d = node_depth(ts, n);
+  int t = n - ts.off[d];
+  return ts.off[d - 1] + t / ts.s[d];
+}
+
+__global__ void __launch_bounds__(kMaxN)
+tree_build_kernel(TreeShape ts, int B, int L_cap, const int32_t* __restrict__ root, const int32_t* __restrict__ topk,
+                  const int32_t* __restrict__ L, int32_t* __restrict__ parent, int32_t* __restrict__ depth,
+                  int32_t* __restrict__ first_child, uint8_t* __restrict__ mask, uint64_t* __restrict__ bits,
+                  int32_t* __restrict__ tokens, int32_t* __restrict__ pos, uint32_t* __restrict__ flags) {
+  const int b = blockIdx.x;
+  const int n = threadIdx.x;
+  const int N = ts.N;
+  const int Lb = L[b];
+  if (n == 0 && flags) flags[b] = (Lb < 0 || Lb + N > L_cap) ? MEDUSA_FLAG_CAPACITY : 0u;
+  if (n >= N) return;
+  const int d = node_depth(ts, n);
+  const int t = n - ts.off[d];
+  const int rank = d > 0 ? t % ts.s[d] : 0;
+  tokens[(size_t)b * N + n] = d == 0 ? root[b] : topk[((size_t)b * ts.K + (d - 1)) * ts.s_max + rank];
+  pos[(size_t)b * N + n] = Lb + d;
+  if (b != 0) return;
+  parent[n] = d > 0 ? ts.off[d - 1] + t / ts.s[d] : -1;
+  depth[n] = d;
+  first_child[n] = d < ts.K ? ts.off[d + 1] + t * ts.s[d + 1] : -1;
+  uint64_t w0 = 0, w1 = 0;
+  for (int j = n; j >= 0; j = node_parent(ts, j)) {
+    if (j < 64) w0 |= 1ull << j;
+    else w1 |= 1ull << (j - 64);
+  }
+  bits[2 * n] = w0;
+  bits[2 * n + 1] = w1;
+  for (int j = 0; j < N; ++j) {
+    uint64_t w = j < 64 ? w0 : w1;
+    mask[(size_t)n * N + j] = uint8_t((w >> (j & 63)) & 1ull);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tree_build(const medusa_cfg& c, const int32_t* root, const int32_t* topk, const int32_t* L,
+                              int32_t* parent, int32_t* depth, int32_t* first_child, uint8_t* mask, uint64_t* bits,
+                              int32_t* tokens, int32_t* pos, uint32_t* flags, cudaStream_t st) {
+  const TreeShape ts = tree_shape(c);
+  tree_build_kernel<<<c.B, kMaxN, 0, st>>>(ts, c.B, c.L_cap, root, topk, L, parent, depth, first_child, mask, bits,
+                                           tokens, pos, flags);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace medusa

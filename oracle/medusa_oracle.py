@@ -312,7 +312,7 @@ def residual(p: np.ndarray, q: np.ndarray) -> np.ndarray:
     return w / tot
 
 
-def inverse_cdf(w: np.ndarray, u: float) -> Tuple[int, bool]:
+def inverse_cdf(w: np.ndarray, u: float, tie: float = CDF_TIE) -> Tuple[int, bool]:
     """Smallest y with sum_{v<=y} w_v > u * sum_v w_v (R10), sequential float64 sums.
 
     Also returns a near-boundary flag: u*total within CDF_TIE*total of the
@@ -322,13 +322,13 @@ def inverse_cdf(w: np.ndarray, u: float) -> Tuple[int, bool]:
     tot = float(c[-1])
     thr = u * tot
     y = int(np.argmax(c > thr))
-    near = abs(thr - c[y]) < CDF_TIE * tot or (y > 0 and abs(thr - c[y - 1]) < CDF_TIE * tot)
+    near = abs(thr - c[y]) < tie * tot or (y > 0 and abs(thr - c[y - 1]) < tie * tot)
     return y, near
 
 
 def verify_rejection(tokens: np.ndarray, parent: np.ndarray, target_logits: np.ndarray,
                      head_logits: np.ndarray, u_acc: np.ndarray, u_res: np.ndarray,
-                     K: int, T: float):
+                     K: int, T: float, rs_tie: float = RS_TIE, cdf_tie: float = CDF_TIE):
     """Tree rejection sampling with the residual carried across siblings (R10).
 
     The single-candidate rule is [MEDUSA-ARCH] "수학적 무손실 보장" and [SPEC-DEC]
@@ -356,14 +356,14 @@ def verify_rejection(tokens: np.ndarray, parent: np.ndarray, target_logits: np.n
             x = int(tokens[c])
             r = acceptance_ratio(p, q, x)
             u = float(u_acc[dep - 1, j])
-            if abs(u - r) < RS_TIE:
+            if abs(u - r) < rs_tie:
                 flags |= FLAG_RS_NEAR_TIE
             if u < r:
                 accepted = c
                 break
             p = residual(p, q)
         if accepted is None:
-            y, near = inverse_cdf(p, float(u_res[dep - 1]))
+            y, near = inverse_cdf(p, float(u_res[dep - 1]), cdf_tie)
             if near:
                 flags |= FLAG_CDF_NEAR_TIE
             out.append(y)
@@ -373,7 +373,7 @@ def verify_rejection(tokens: np.ndarray, parent: np.ndarray, target_logits: np.n
         path.append(cur)
         out.append(int(tokens[cur]))
         p = softmax_t(target_logits[cur], T)
-    y, near = inverse_cdf(p, float(u_res[K]))
+    y, near = inverse_cdf(p, float(u_res[K]), cdf_tie)
     if near:
         flags |= FLAG_CDF_NEAR_TIE
     out.append(y)
@@ -382,7 +382,8 @@ def verify_rejection(tokens: np.ndarray, parent: np.ndarray, target_logits: np.n
 
 
 def verify_batch(mode: int, tree: dict, target_logits: np.ndarray, K: int,
-                 head_logits: Optional[np.ndarray] = None, u_acc=None, u_res=None, T: float = 1.0):
+                 head_logits: Optional[np.ndarray] = None, u_acc=None, u_res=None, T: float = 1.0,
+                 rs_tie: float = RS_TIE, cdf_tie: float = CDF_TIE):
     """Run the walk for every sequence. mode 0 = greedy, 1 = rejection sampling."""
     B = target_logits.shape[0]
     acc = np.zeros(B, dtype=np.int64)
@@ -396,7 +397,7 @@ def verify_batch(mode: int, tree: dict, target_logits: np.ndarray, K: int,
             f = 0
         else:
             a, pth, o, n, f = verify_rejection(tree["tokens"][b], tree["parent"], target_logits[b],
-                                               head_logits[b], u_acc[b], u_res[b], K, T)
+                                               head_logits[b], u_acc[b], u_res[b], K, T, rs_tie, cdf_tie)
         acc[b], path[b], outt[b], n_out[b], flags[b] = a, pth, o, n, f
     return {"acc": acc, "path": path, "out_tokens": outt, "n_out": n_out, "flags": flags}
 

@@ -1,0 +1,102 @@
+"""The C ABI library loads on the host and exports what include/medusa.h declares (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from medusa_speculative_decoding_heads_gb300 import _build, binding as mb, configs
+from medusa_speculative_decoding_heads_gb300.step import cfg_for
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return mb.load()
+
+
+def declared_entry_points():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^MEDUSA_API\s+(?:int|uint64_t|const char\*)\s+(medusa_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_header_declares_the_five_steps():
+    names = declared_entry_points()
+    for n in ("medusa_heads", "medusa_tree_build", "medusa_tree_attention", "medusa_verify", "medusa_kv_compact"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_entry_points():
+        assert hasattr(lib, name), name
+
+
+def test_binding_lists_every_declared_entry_point():
+    assert set(mb.ENTRY_POINTS) == declared_entry_points()
+
+
+def test_status_strings(lib):
+    assert mb.status_string(0) == "ok"
+    assert mb.status_string(-1) == "invalid argument"
+    assert mb.status_string(-2) == "unsupported configuration"
+
+
+def test_node_count_and_workspace(lib):
+    for name in configs.ORDER:
+        w = configs.get(name)
+        cfg = cfg_for(w, L_cap=w.L_range[1] + w.N, mode=w.modes[0])
+        assert mb.node_count(cfg) == w.N
+        assert mb.workspace_size(cfg) > 0
+
+
+def _cfg(**kw):
+    w = configs.get("tiny_fp32")
+    cfg = cfg_for(w, L_cap=256, mode=configs.GREEDY)
+    for k, v in kw.items():
+        setattr(cfg, k, v)
+    return cfg
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("K", 0, -1), ("K", 9, -2), ("D", 96, -2), ("Hkv", 3, -2), ("dtype", 5, -1), ("mode", 7, -1),
+    ("L_cap", 10, -3), ("B", 0, -1),
+])
+def test_bad_configs_are_rejected_before_any_launch(lib, field, value, status):
+    cfg = _cfg(**{field: value})
+    n = ctypes.c_size_t()
+    assert lib.medusa_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == status
+
+
+def test_too_many_nodes_and_wide_branching(lib):
+    cfg = _cfg(K=4)
+    for i, s in enumerate((8, 8, 1, 1)):
+        cfg.branching[i] = s
+    assert mb.raw_call("medusa_workspace_size", ctypes.byref(cfg), ctypes.byref(ctypes.c_size_t())) == -2
+    cfg = _cfg()
+    cfg.branching[0] = 9
+    assert mb.raw_call("medusa_workspace_size", ctypes.byref(cfg), ctypes.byref(ctypes.c_size_t())) == -2
+
+
+def test_null_pointers_are_rejected(lib):
+    cfg = _cfg()
+    assert lib.medusa_heads(ctypes.byref(cfg), None, None, None, None, None, None, None, None) == -1
+    assert lib.medusa_tree_build(ctypes.byref(cfg), *([None] * 12)) == -1
+    assert lib.medusa_tree_attention(ctypes.byref(cfg), *([None] * 8)) == -1
+    assert lib.medusa_verify(ctypes.byref(cfg), *([None] * 13)) == -1
+    assert lib.medusa_kv_compact(ctypes.byref(cfg), *([None] * 7)) == -1
+    rs = _cfg(mode=configs.REJECTION, temperature=0.0)
+    assert lib.medusa_workspace_size(ctypes.byref(rs), ctypes.byref(ctypes.c_size_t())) == -1
+
+
+def test_rejection_mode_needs_logits_and_uniforms(lib):
+    cfg = _cfg(mode=configs.REJECTION)
+    fake = ctypes.c_void_p(256)   # never dereferenced: validation fails first
+    assert lib.medusa_heads(ctypes.byref(cfg), fake, fake, None, fake, None, fake, fake, None) == -1
+    assert lib.medusa_verify(ctypes.byref(cfg), fake, fake, fake, fake, None, None, None, fake, fake, fake, fake,
+                             fake, None) == -1

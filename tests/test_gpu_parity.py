@@ -1,0 +1,328 @@
+"""GPU parity: every library call against the float64 oracle on identical seeded inputs.
+
+Integer outputs (tree arrays, tokens, positions, top-s indices, acceptance,
+paths, KV map, compacted KV bytes) must match bit for bit, except where the
+oracle flags a near tie that float32 may legitimately order differently.
+Float outputs (head logits, attention) must satisfy
+|gpu - oracle| <= tol * max(1, |oracle|) with tol = 1e-5 (float32) or 2e-2 (bf16).
+"""
+import numpy as np
+import pytest
+import torch
+
+from medusa_speculative_decoding_heads_gb300 import binding as mb, configs, synth
+from medusa_speculative_decoding_heads_gb300.configs import BF16, F32, GREEDY, REJECTION
+from medusa_speculative_decoding_heads_gb300.step import DeviceStep, to_device_inputs
+from oracle import medusa_oracle as O
+
+from _helpers import assert_close, f64, gpu_ready, i64, planted_greedy_logits, random_topk
+
+pytestmark = pytest.mark.gpu
+
+NAMES = configs.ORDER
+
+
+def small(w):
+    """A reduced case of workload w: same dtype, tree and batch; ragged sizes that span several tiles."""
+    if w.name == "tiny_fp32":
+        return w
+    G = w.Hq // w.Hkv
+    return configs.scaled(w, d=512, V=1000, Hq=2 * G, Hkv=2, L_range=(37, 300))
+
+
+def oracle_tree(w, root, topk, L, L_cap):
+    return O.tree_build(w.branching, np.asarray(root), np.asarray(topk), np.asarray(L), L_cap)
+
+
+# --------------------------------------------------------------------------- tree build
+@pytest.mark.parametrize("name", NAMES)
+def test_tree_build_bit_exact(name):
+    dev = gpu_ready()
+    w = configs.get(name)
+    rng = np.random.default_rng(1)
+    L = synth.committed_lengths(3, w.B, *w.L_range)
+    L_cap = synth.cache_capacity(L, w.N)
+    L[-1] = L_cap - w.N + 1                      # one sequence over capacity
+    root = synth.root_tokens(3, w.B, w.V)
+    topk = random_topk(rng, w.B, w.K, w.s_max, w.branching, w.V)
+    st = DeviceStep(w, w.modes[0], L_cap, dev)
+    t_topk = torch.from_numpy(topk).to(dev)
+    st.tree_build(torch.from_numpy(root).to(dev), torch.from_numpy(L).to(dev), topk=t_topk)
+    torch.cuda.synchronize()
+    ref = oracle_tree(w, root, topk, L, L_cap)
+    assert np.array_equal(i64(st.parent), ref["parent"])
+    assert np.array_equal(i64(st.depth), ref["depth"])
+    assert np.array_equal(i64(st.first_child), ref["first_child"])
+    assert np.array_equal(i64(st.mask), ref["mask"].astype(np.int64))
+    assert np.array_equal(st.anc_bits.cpu().numpy().view(np.uint64), ref["anc_bits"])
+    assert np.array_equal(i64(st.tokens), ref["tokens"])
+    assert np.array_equal(i64(st.pos), ref["pos"])
+    assert np.array_equal(i64(st.flags), ref["flags"])
+
+
+# --------------------------------------------------------------------------- heads
+def check_heads(w, si, st, rows=None):
+    """Compare logits and top-s of (b, k) pairs (all when rows is None)."""
+    h, W, U = f64(si.h), None, None
+    pairs = rows if rows is not None else [(b, k) for b in range(w.B) for k in range(w.K)]
+    z_gpu = st.logits.cpu().numpy()
+    topk_gpu = st.topk.cpu().numpy()
+    worst = 0.0
+    checked = flagged = 0
+    for k in sorted({k for _, k in pairs}):
+        Wk = f64(si.W[k:k + 1])
+        bk = None if si.bias is None else f64(si.bias[k:k + 1])
+        Uk = f64(si.U[k:k + 1])
+        bs = sorted({b for b, kk in pairs if kk == k})
+        _, z = O.medusa_heads(h[bs], Wk, bk, Uk)
+        for j, b in enumerate(bs):
+            worst = max(worst, assert_close(z_gpu[b, k], z[j, 0], w.dtype, f"logits b={b} k={k}"))
+            idx, near = O.top_s(z[j, 0], w.branching[k])
+            if near:
+                flagged += 1
+                continue
+            checked += 1
+            assert list(topk_gpu[b, k, :w.branching[k]]) == list(idx), f"top-s b={b} k={k}"
+            assert all(v == -1 for v in topk_gpu[b, k, w.branching[k]:])
+    assert checked > 0 and flagged <= max(1, len(pairs) // 10)
+    return worst
+
+
+@pytest.mark.parametrize("name", NAMES)
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_heads_small(name, with_bias):
+    dev = gpu_ready()
+    w = small(configs.get(name))
+    si = synth.make_step_inputs(w, seed=11, device=dev, with_bias=with_bias)
+    st = DeviceStep(w, w.modes[0], si.L_cap, dev)
+    st.heads(si.h, si.W, si.bias, si.U)
+    torch.cuda.synchronize()
+    check_heads(w, si, st)
+
+
+@pytest.mark.parametrize("B", [1, 3, 9, 17, 32])
+def test_heads_batch_tiles(B):
+    """Every batch tiling of the tensor-core path (1, 2 and 4 tiles of 8) with ragged batches."""
+    dev = gpu_ready()
+    w = configs.scaled(configs.get("vicuna7b_b1"), B=B, d=320, V=700, L_range=(40, 40), Hq=2, Hkv=2)
+    si = synth.make_step_inputs(w, seed=B, device=dev, with_bias=True)
+    st = DeviceStep(w, GREEDY, si.L_cap, dev)
+    st.heads(si.h, si.W, si.bias, si.U)
+    torch.cuda.synchronize()
+    check_heads(w, si, st)
+
+
+@pytest.mark.parametrize("name", NAMES[1:])
+def test_heads_full_size_sampled(name):
+    dev = gpu_ready()
+    w = configs.get(name)
+    si = synth.make_step_inputs(configs.scaled(w, L_range=(64, 64), Hq=w.Hq // w.Hkv, Hkv=1), seed=5, device=dev)
+    st = DeviceStep(w, w.modes[0], si.L_cap, dev)
+    st.heads(si.h, si.W, si.bias, si.U)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    pairs = [(int(rng.integers(w.B)), k) for k in (0, w.K - 1)]
+    check_heads(w, si, st, rows=pairs)
+
+
+# --------------------------------------------------------------------------- attention
+def check_attention(w, si, O_gpu, pairs):
+    tree = O.tree_layout(w.branching)
+    mask = O.ancestor_mask(tree["parent"])
+    G = w.Hq // w.Hkv
+    worst = 0.0
+    for b, kv in pairs:
+        Lb = int(si.L[b])
+        q = f64(si.Q[b:b + 1, :, kv * G:(kv + 1) * G])
+        kc = f64(si.Kc[b:b + 1, kv:kv + 1, :Lb + w.N])
+        vc = f64(si.Vc[b:b + 1, kv:kv + 1, :Lb + w.N])
+        ref = O.tree_attention(q, kc, vc, np.array([Lb]), mask, G, 1)
+        got = f64(O_gpu[b:b + 1, :, kv * G:(kv + 1) * G])
+        worst = max(worst, assert_close(got, ref, w.dtype, f"attention b={b} kv={kv}"))
+    return worst
+
+
+def run_attention(w, si, dev):
+    st = DeviceStep(w, w.modes[0], si.L_cap, dev)
+    st.tree_build(torch.from_numpy(si.root_token).to(dev), torch.from_numpy(si.L).to(dev),
+                  topk=torch.zeros((w.B, w.K, w.s_max), dtype=torch.int32, device=dev))
+    st.tree_attention(si.Q, si.Kc, si.Vc, torch.from_numpy(si.L).to(dev))
+    torch.cuda.synchronize()
+    return st
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_attention_small_all_heads(name):
+    dev = gpu_ready()
+    w = small(configs.get(name))
+    si = synth.make_step_inputs(w, seed=21, device=dev)
+    st = run_attention(w, si, dev)
+    check_attention(w, si, st.O, [(b, kv) for b in range(w.B) for kv in range(w.Hkv)])
+
+
+@pytest.mark.parametrize("L0", [0, 1, 31, 32, 33, 511])
+def test_attention_edge_lengths(L0):
+    """Empty prefix, a single key, tile boundaries."""
+    dev = gpu_ready()
+    w = configs.scaled(configs.get("gqa7b_b32"), B=2, d=64, V=64, L_range=(L0, L0))
+    si = synth.make_step_inputs(w, seed=L0, device=dev)
+    st = run_attention(w, si, dev)
+    check_attention(w, si, st.O, [(b, kv) for b in range(w.B) for kv in range(w.Hkv)])
+
+
+@pytest.mark.parametrize("name", NAMES[1:])
+def test_attention_full_size_sampled(name):
+    dev = gpu_ready()
+    w = configs.get(name)
+    si = synth.make_step_inputs(configs.scaled(w, d=64, V=64), seed=7, device=dev)
+    st = run_attention(w, si, dev)
+    rng = np.random.default_rng(3)
+    pairs = [(int(rng.integers(w.B)), int(rng.integers(w.Hkv))) for _ in range(3)] + [(w.B - 1, w.Hkv - 1)]
+    check_attention(w, si, st.O, pairs)
+
+
+# --------------------------------------------------------------------------- verify
+def greedy_case(w, dev, seed):
+    rng = np.random.default_rng(seed)
+    L = synth.committed_lengths(seed, w.B, *w.L_range)
+    L_cap = synth.cache_capacity(L, w.N)
+    root = synth.root_tokens(seed, w.B, w.V)
+    topk = random_topk(rng, w.B, w.K, w.s_max, w.branching, w.V)
+    tree = oracle_tree(w, root, topk, L, L_cap)
+    tl = synth.target_logits(w, seed, device=dev)
+    depths = planted_greedy_logits(tl, tree, seed, w.K)
+    return L, L_cap, root, topk, tree, tl, depths
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_verify_greedy_bit_exact(name):
+    dev = gpu_ready()
+    w = configs.scaled(configs.get(name), B=max(configs.get(name).B, 12), target_corr=0.0)
+    L, L_cap, root, topk, tree, tl, depths = greedy_case(w, dev, seed=5)
+    st = DeviceStep(w, GREEDY, L_cap, dev)
+    st.tree_build(torch.from_numpy(root).to(dev), torch.from_numpy(L).to(dev), topk=torch.from_numpy(topk).to(dev))
+    st.verify(tl)
+    torch.cuda.synchronize()
+    ref = O.verify_batch(GREEDY, tree, f64(tl), w.K)
+    for key in ("acc", "path", "out_tokens", "n_out"):
+        assert np.array_equal(i64(getattr(st, key)), ref[key]), key
+    assert np.array_equal(i64(st.flags), np.zeros(w.B))
+    assert (ref["acc"] >= np.array(depths)).all()
+    assert len(set(ref["acc"].tolist())) > 1
+
+
+def rs_case(w, dev, seed, sigma_head=2.0):
+    """Stand-in head logits (float32) and correlated target logits, identical for both sides."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    z = torch.randn((w.B, w.K, w.V), generator=gen, device=dev) * sigma_head
+    L = synth.committed_lengths(seed, w.B, *w.L_range)
+    L_cap = synth.cache_capacity(L, w.N)
+    root = synth.root_tokens(seed, w.B, w.V)
+    topk, _ = O.heads_top_s(z.double().cpu().numpy(), w.branching)
+    tree = oracle_tree(w, root, topk.astype(np.int32), L, L_cap)
+    corr = configs.scaled(w, target_corr=max(w.target_corr, 0.8))
+    tl = synth.target_logits(corr, seed, device=dev, zhat=z, depth=tree["depth"])
+    u_acc, u_res = synth.uniforms_for_step(seed, w.B, w.K, w.s_max)
+    return L, L_cap, root, topk.astype(np.int32), tree, tl, z, u_acc, u_res
+
+
+@pytest.mark.parametrize("name,T", [("tiny_fp32", 1.0), ("vicuna13b_b8", 1.0), ("gqa7b_b32", 0.7),
+                                    ("vicuna7b_b1", 0.5), ("vicuna33b_b16", 1.3)])
+def test_verify_rejection_decisions(name, T):
+    dev = gpu_ready()
+    w = configs.scaled(configs.get(name), temperature=T)
+    if w.B < 16:
+        w = configs.scaled(w, B=16)
+    total_acc = 0
+    for seed in (1, 2):
+        L, L_cap, root, topk, tree, tl, z, u_acc, u_res = rs_case(w, dev, seed)
+        st = DeviceStep(w, REJECTION, L_cap, dev)
+        st.tree_build(torch.from_numpy(root).to(dev), torch.from_numpy(L).to(dev),
+                      topk=torch.from_numpy(topk).to(dev))
+        st.verify(tl, torch.from_numpy(u_acc).to(dev), torch.from_numpy(u_res).to(dev), head_logits=z)
+        torch.cuda.synchronize()
+        ref = O.verify_batch(REJECTION, tree, f64(tl), w.K, head_logits=f64(z), u_acc=u_acc, u_res=u_res, T=T)
+        gflags = i64(st.flags)
+        for b in range(w.B):
+            if ref["flags"][b] or gflags[b]:
+                assert 1 <= int(st.n_out[b]) <= w.K + 1
+                continue
+            for key in ("acc", "path", "out_tokens", "n_out"):
+                assert np.array_equal(i64(getattr(st, key))[b], ref[key][b]), (key, b, seed)
+        total_acc += int(ref["acc"].sum())
+    assert total_acc > 0
+
+
+# --------------------------------------------------------------------------- compaction
+@pytest.mark.parametrize("name", NAMES)
+def test_kv_compact_bit_exact(name):
+    dev = gpu_ready()
+    w = small(configs.get(name))
+    si = synth.make_step_inputs(w, seed=9, device=dev)
+    rng = np.random.default_rng(9)
+    tree = O.tree_layout(w.branching)
+    acc = rng.integers(0, w.K + 1, size=w.B).astype(np.int32)
+    acc[0] = 0
+    acc[-1] = w.K
+    path = np.full((w.B, w.K + 1), -1, dtype=np.int32)
+    for b in range(w.B):
+        cur = 0
+        path[b, 0] = 0
+        for r in range(1, acc[b] + 1):
+            kids = O.children_of(tree["parent"], cur)
+            cur = kids[int(rng.integers(len(kids)))]
+            path[b, r] = cur
+    L = si.L.copy()
+    raw = lambda t: t.cpu().view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32).numpy()
+    k0, v0 = raw(si.Kc), raw(si.Vc)
+    st = DeviceStep(w, w.modes[0], si.L_cap, dev)
+    st.acc.copy_(torch.from_numpy(acc))
+    st.path.copy_(torch.from_numpy(path))
+    Ld = torch.from_numpy(L).to(dev)
+    st.kv_compact(si.Kc, si.Vc, Ld)
+    torch.cuda.synchronize()
+    kr, vr, Lr, kv_map = O.kv_compact(k0, v0, L, acc, path)
+    assert np.array_equal(raw(si.Kc), kr) and np.array_equal(raw(si.Vc), vr)
+    assert np.array_equal(i64(Ld), Lr) and np.array_equal(i64(st.kv_map), kv_map)
+
+
+# --------------------------------------------------------------------------- whole step
+@pytest.mark.parametrize("name", NAMES)
+def test_step_end_to_end_small(name):
+    """The five calls in order on one stream against the oracle's step on the same inputs."""
+    dev = gpu_ready()
+    w = small(configs.get(name))
+    if w.B < 8:
+        w = configs.scaled(w, B=8)
+    for mode in w.modes:
+        si = synth.make_step_inputs(w, seed=31, device=dev, with_bias=True)
+        r, z = O.medusa_heads(f64(si.h), f64(si.W), f64(si.bias), f64(si.U))
+        topk_ref, near = O.heads_top_s(z, w.branching)
+        tree = oracle_tree(w, si.root_token, topk_ref, si.L, si.L_cap)
+        if mode == REJECTION:
+            tl = synth.target_logits(configs.scaled(w, target_corr=0.8), 31, device=dev,
+                                     zhat=torch.from_numpy(z).float(), depth=tree["depth"])
+        else:
+            tl = synth.target_logits(w, 31, device=dev)
+            planted_greedy_logits(tl, tree, 31, w.K)
+        inp = to_device_inputs(si, tl, dev)
+        Kc0, Vc0 = f64(si.Kc), f64(si.Vc)
+        st = DeviceStep(w, mode, si.L_cap, dev)
+        st.run(inp, write_logits=True, compact=True)
+        torch.cuda.synchronize()
+        assert_close(st.logits.cpu().numpy(), z, w.dtype, "logits")
+        ok_b = ~near.any(axis=1)
+        assert np.array_equal(i64(st.topk)[ok_b], topk_ref[ok_b])
+        assert np.array_equal(i64(st.tokens)[ok_b], tree["tokens"][ok_b])
+        Oref = O.tree_attention(f64(si.Q), Kc0, Vc0, si.L, tree["mask"], w.Hq, w.Hkv)
+        assert_close(f64(st.O), Oref, w.dtype, "attention")
+        ver = O.verify_batch(mode, tree, f64(tl), w.K, head_logits=z, u_acc=si.u_acc, u_res=si.u_res,
+                             T=w.temperature, rs_tie=1e-5, cdf_tie=1e-5)
+        ok = ok_b & (ver["flags"] == 0)
+        for key in ("acc", "path", "out_tokens", "n_out"):
+            assert np.array_equal(i64(getattr(st, key))[ok], ver[key][ok]), key
+        kr, vr, Lr, kv_map = O.kv_compact(Kc0, Vc0, si.L, ver["acc"], ver["path"])
+        assert np.array_equal(i64(inp.L)[ok], Lr[ok]) and np.array_equal(i64(st.kv_map)[ok], kv_map[ok])
+        assert np.array_equal(f64(inp.Kc)[ok], kr[ok]) and np.array_equal(f64(inp.Vc)[ok], vr[ok])
+        assert ok.sum() >= max(1, w.B // 2)
