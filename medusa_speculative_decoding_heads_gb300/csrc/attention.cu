@@ -31,20 +31,37 @@ struct AttnPlan {
   size_t o_part, ml_part, total;
 };
 
+// Kernel choice: float32 -> CUDA cores; bf16 with D = 128 -> tcgen05; bf16 with D = 64 -> mma.sync.
+enum AttnPath { kPathF32 = 0, kPathMma = 1, kPathTc = 2 };
+
+int attention_path(const medusa_cfg& c) {
+  if (c.dtype == MEDUSA_F32) return kPathF32;
+  return c.D == 128 ? kPathTc : kPathMma;
+}
+
 AttnPlan plan_attention(const medusa_cfg& c) {
   AttnPlan p{};
   const TreeShape ts = tree_shape(c);
   p.G = c.Hq / c.Hkv;
   p.NG = ts.N * p.G;
-  if (c.dtype == MEDUSA_BF16) attention_mma_warps(p.NG, &p.row_groups);
-  else p.row_groups = (p.NG + kRowsPerCta - 1) / kRowsPerCta;
+  const int path = attention_path(c);
+  int tile = kKeyTile;
+  if (path == kPathTc) {
+    p.row_groups = attention_tc_mtiles(p.NG);
+    tile = 128;
+  } else if (path == kPathMma) {
+    attention_mma_warps(p.NG, &p.row_groups);
+    tile = 64;
+  } else {
+    p.row_groups = (p.NG + kRowsPerCta - 1) / kRowsPerCta;
+  }
   const int Lmax = c.L_cap - ts.N;   // longest committed prefix that fits
   const long ctas = (long)p.row_groups * c.Hkv * c.B;
   int want = (int)((2L * 152 + ctas - 1) / ctas);
   int by_len = (Lmax + 255) / 256;
   p.nsplit = want < by_len ? want : by_len;
   if (p.nsplit < 1) p.nsplit = 1;
-  p.chunk = Lmax > 0 ? ((Lmax + p.nsplit - 1) / p.nsplit + kKeyTile - 1) / kKeyTile * kKeyTile : kKeyTile;
+  p.chunk = Lmax > 0 ? ((Lmax + p.nsplit - 1) / p.nsplit + tile - 1) / tile * tile : tile;
   const size_t rows = (size_t)c.B * p.nsplit * ts.N * c.Hq;
   size_t off = 0;
   p.o_part = off;
@@ -213,7 +230,10 @@ cudaError_t run(const medusa_cfg& c, const AttnPlan& p, const void* Q, const voi
   float* o_part = reinterpret_cast<float*>(ws + p.o_part);
   float* ml_part = reinterpret_cast<float*>(ws + p.ml_part);
   cudaError_t e;
-  if (c.dtype == MEDUSA_BF16) {
+  const int path = attention_path(c);
+  if (path == kPathTc) {
+    e = launch_attention_tc(c, p.nsplit, p.chunk, Q, Kc, Vc, L, bits, o_part, ml_part, st);
+  } else if (path == kPathMma) {
     e = launch_attention_mma(c, p.nsplit, p.chunk, Q, Kc, Vc, L, bits, o_part, ml_part, st);
   } else {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));

@@ -85,6 +85,10 @@ cudaError_t launch_attention(const medusa_cfg& c, const void* Q, const void* Kc,
                              const int32_t* L, const uint64_t* bits, void* O, void* ws, cudaStream_t st);
 size_t attention_workspace(const medusa_cfg& c);
 int attention_mma_warps(int NG, int* row_blocks);
+int attention_tc_mtiles(int NG);
+cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, const void* Q, const void* Kc,
+                                const void* Vc, const int32_t* L, const uint64_t* bits, float* o_part, float* ml_part,
+                                cudaStream_t st);
 cudaError_t launch_attention_mma(const medusa_cfg& c, int nsplit, int chunk, const void* Q, const void* Kc,
                                  const void* Vc, const int32_t* L, const uint64_t* bits, float* o_part, float* ml_part,
                                  cudaStream_t st);

@@ -160,11 +160,12 @@ def test_attention_small_all_heads(name):
     check_attention(w, si, st.O, [(b, kv) for b in range(w.B) for kv in range(w.Hkv)])
 
 
-@pytest.mark.parametrize("L0", [0, 1, 31, 32, 33, 511])
-def test_attention_edge_lengths(L0):
-    """Empty prefix, a single key, tile boundaries."""
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("L0", [0, 1, 31, 32, 33, 127, 128, 129, 511])
+def test_attention_edge_lengths(L0, D):
+    """Empty prefix, a single key, tile boundaries of every kernel (32/64/128-key tiles)."""
     dev = gpu_ready()
-    w = configs.scaled(configs.get("gqa7b_b32"), B=2, d=64, V=64, L_range=(L0, L0))
+    w = configs.scaled(configs.get("gqa7b_b32"), B=2, d=64, V=64, L_range=(L0, L0), D=D)
     si = synth.make_step_inputs(w, seed=L0, device=dev)
     st = run_attention(w, si, dev)
     check_attention(w, si, st.O, [(b, kv) for b in range(w.B) for kv in range(w.Hkv)])
