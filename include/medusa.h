@@ -172,6 +172,31 @@ MEDUSA_API int medusa_verify(const medusa_cfg* cfg, const int32_t* tokens, const
 MEDUSA_API int medusa_kv_compact(const medusa_cfg* cfg, void* Kc, void* Vc, int32_t* L, const int32_t* acc,
                       const int32_t* path, int32_t* kv_map, medusa_stream_t stream);
 
+/* Tree attention for callers that cannot allocate device memory.
+ * No counterpart on the source pages: this is a deployment variant of
+ * medusa_tree_attention for callers that cannot call cudaMalloc (for example a
+ * serving engine that reserved nearly all device memory for its KV cache at
+ * start-up and forbids later allocations, or a plug-in inside a framework whose
+ * allocator owns every device byte). Arguments, layouts and results are those
+ * of medusa_tree_attention; there is no workspace argument. The split-KV
+ * partial results live instead in one static device array of
+ * MEDUSA_NOALLOC_SCRATCH_BYTES that the library holds on every GPU that loads
+ * it, until the process exits.
+ *   - Returns MEDUSA_ERR_UNSUPPORTED, enqueueing nothing, when the
+ *     configuration needs more scratch than that (medusa_workspace_size
+ *     minus the heads part; B * N * Hq * (D + 2) * 4 bytes per KV split).
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call uses the same array: calls whose kernels may overlap on the
+ *     GPU (other streams, concurrent graph replays) race and must not be
+ *     issued. Each call writes all the scratch it reads. */
+#define MEDUSA_NOALLOC_SCRATCH_BYTES (64u << 20)
+MEDUSA_API int medusa_tree_attention_noalloc(const medusa_cfg* cfg, const void* Q, const void* Kc, const void* Vc,
+                                             const int32_t* L, const uint64_t* anc_bits, void* O,
+                                             medusa_stream_t stream);
+
 /* Number of kernels this library has enqueued in this process so far (host-side
  * counter, for diagnostics; no counterpart on the pages). */
 MEDUSA_API uint64_t medusa_launch_count(void);

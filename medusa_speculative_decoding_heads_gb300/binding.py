@@ -20,8 +20,8 @@ GREEDY, REJECTION = 0, 1
 FLAG_RS_NEAR_TIE, FLAG_CDF_NEAR_TIE, FLAG_CAPACITY = 1, 2, 4
 
 ENTRY_POINTS = ("medusa_node_count", "medusa_workspace_size", "medusa_heads", "medusa_tree_build",
-                "medusa_tree_attention", "medusa_verify", "medusa_kv_compact", "medusa_launch_count",
-                "medusa_status_string")
+                "medusa_tree_attention", "medusa_verify", "medusa_kv_compact", "medusa_tree_attention_noalloc",
+                "medusa_launch_count", "medusa_status_string")
 
 
 class MedusaError(RuntimeError):
@@ -67,6 +67,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "medusa_heads": [cp, P, P, P, P, P, P, P, P],
         "medusa_tree_build": [cp, P, P, P, P, P, P, P, P, P, P, P, P],
         "medusa_tree_attention": [cp, P, P, P, P, P, P, P, P],
+        "medusa_tree_attention_noalloc": [cp, P, P, P, P, P, P, P],
         "medusa_verify": [cp, P, P, P, P, P, P, P, P, P, P, P, P, P],
         "medusa_kv_compact": [cp, P, P, P, P, P, P, P],
     }
@@ -141,6 +142,12 @@ def tree_attention(cfg, Q, Kc, Vc, L, anc_bits, O, workspace, stream=None):
     _check("medusa_tree_attention", load().medusa_tree_attention(
         ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), _ptr(L), _ptr(anc_bits), _ptr(O), _ptr(workspace),
         _stream(stream)))
+
+
+def tree_attention_noalloc(cfg, Q, Kc, Vc, L, anc_bits, O, stream=None):
+    """medusa_tree_attention with the library's static scratch instead of a workspace."""
+    _check("medusa_tree_attention_noalloc", load().medusa_tree_attention_noalloc(
+        ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), _ptr(L), _ptr(anc_bits), _ptr(O), _stream(stream)))
 
 
 def verify(cfg, tokens, parent, first_child, target_logits, head_logits, u_acc, u_res, acc, path, out_tokens,

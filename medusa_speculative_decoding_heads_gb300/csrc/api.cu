@@ -43,6 +43,9 @@ int check_cfg(const medusa_cfg* c) {
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? MEDUSA_OK : MEDUSA_ERR_CUDA; }
 
 }  // namespace
+
+int check_cfg_public(const medusa_cfg* c) { return check_cfg(c); }
+
 }  // namespace medusa
 
 using namespace medusa;

@@ -103,6 +103,9 @@ cudaError_t launch_kv_compact(const medusa_cfg& c, void* Kc, void* Vc, int32_t* 
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Configuration checks shared by every entry point (MEDUSA_OK or an error status).
+int check_cfg_public(const medusa_cfg* c);
+
 // Host-side count of kernels this library has enqueued (diagnostics).
 void note_launches(int n);
 
