@@ -91,9 +91,9 @@ typedef struct {
 /* Node count N of the configured tree. Host only; `N` is a host pointer. */
 MEDUSA_API int medusa_node_count(const medusa_cfg* cfg, int32_t* N);
 
-/* Workspace bytes needed by medusa_heads and medusa_tree_attention for this
- * configuration (one workspace may serve both, since they use disjoint parts).
- * Host only; `bytes` is a host pointer. */
+/* Workspace bytes needed by medusa_heads, medusa_tree_attention and
+ * medusa_verify for this configuration (one workspace serves all three: they
+ * use disjoint parts). Host only; `bytes` is a host pointer. */
 MEDUSA_API int medusa_workspace_size(const medusa_cfg* cfg, size_t* bytes);
 
 /* Step 1 — Medusa heads and per-head top-s.
@@ -106,7 +106,8 @@ MEDUSA_API int medusa_workspace_size(const medusa_cfg* cfg, size_t* bytes);
  *                              `head_logits` by medusa_verify in MEDUSA_REJECTION.
  *   topk   [B][K][s_max] int32 indices of the s_k largest z_k entries, descending,
  *                              ties to the lower index; -1 beyond s_k.
- * r_k is kept in float32; accumulation is float32. */
+ * r_k is kept in float32; accumulation is float32. bf16 needs d % 64 == 0 and
+ * B <= 32 (MEDUSA_ERR_UNSUPPORTED otherwise). */
 MEDUSA_API int medusa_heads(const medusa_cfg* cfg, const void* h, const void* W, const void* bias,
                  const void* U, float* logits, int32_t* topk, void* workspace,
                  medusa_stream_t stream);
@@ -146,10 +147,14 @@ MEDUSA_API int medusa_tree_attention(const medusa_cfg* cfg, const void* Q, const
  *   head_logits [B][K][V] float   z from medusa_heads (MEDUSA_REJECTION only, else NULL)
  *   u_acc [B][K][s_max] float     acceptance uniforms (REJECTION only, else NULL)
  *   u_res [B][K+1] float          resampling uniforms (REJECTION only, else NULL)
+ *   workspace                     as for medusa_heads (256-byte aligned)
  * Outputs: acc [B] accepted drafts; path [B][K+1] node ids (path[0] = 0, -1 pad);
  *   out_tokens [B][K+1] the accepted tokens then the bonus/correction token
  *   (-1 pad); n_out [B] = acc + 1; flags [B] uint32: this call ORs in its
  *   MEDUSA_FLAG_* bits (clear or initialise it first, e.g. with medusa_tree_build).
+ * Every tree node's target row is reduced in parallel first (argmax, or row max
+ * and softmax normaliser), so the serial walk only sweeps rows on rejection
+ * and for the final draw.
  * GREEDY: the child whose token equals argmax(target_logits[node]) (ties to
  * the lowest id) is accepted until none matches; the bonus is that argmax at
  * the last accepted node.
@@ -161,7 +166,8 @@ MEDUSA_API int medusa_tree_attention(const medusa_cfg* cfg, const void* Q, const
 MEDUSA_API int medusa_verify(const medusa_cfg* cfg, const int32_t* tokens, const int32_t* parent,
                   const int32_t* first_child, const void* target_logits, const float* head_logits,
                   const float* u_acc, const float* u_res, int32_t* acc, int32_t* path,
-                  int32_t* out_tokens, int32_t* n_out, uint32_t* flags, medusa_stream_t stream);
+                  int32_t* out_tokens, int32_t* n_out, uint32_t* flags, void* workspace,
+                             medusa_stream_t stream);
 
 /* Step 5 — KV compaction of the accepted path, in place.
  *   Kc, Vc [B][Hkv][L_cap][D] elt: for r = 0..acc_b, row L_b + r <- row L_b + path[b][r]

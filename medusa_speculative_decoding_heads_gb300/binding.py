@@ -68,7 +68,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "medusa_tree_build": [cp, P, P, P, P, P, P, P, P, P, P, P, P],
         "medusa_tree_attention": [cp, P, P, P, P, P, P, P, P],
         "medusa_tree_attention_noalloc": [cp, P, P, P, P, P, P, P],
-        "medusa_verify": [cp, P, P, P, P, P, P, P, P, P, P, P, P, P],
+        "medusa_verify": [cp, P, P, P, P, P, P, P, P, P, P, P, P, P, P],
         "medusa_kv_compact": [cp, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
@@ -151,11 +151,11 @@ def tree_attention_noalloc(cfg, Q, Kc, Vc, L, anc_bits, O, stream=None):
 
 
 def verify(cfg, tokens, parent, first_child, target_logits, head_logits, u_acc, u_res, acc, path, out_tokens,
-           n_out, flags, stream=None):
+           n_out, flags, workspace, stream=None):
     _check("medusa_verify", load().medusa_verify(
         ctypes.byref(cfg), _ptr(tokens), _ptr(parent), _ptr(first_child), _ptr(target_logits), _ptr(head_logits),
         _ptr(u_acc), _ptr(u_res), _ptr(acc), _ptr(path), _ptr(out_tokens), _ptr(n_out), _ptr(flags),
-        _stream(stream)))
+        _ptr(workspace), _stream(stream)))
 
 
 def kv_compact(cfg, Kc, Vc, L, acc, path, kv_map, stream=None):

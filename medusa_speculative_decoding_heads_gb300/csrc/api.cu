@@ -64,7 +64,7 @@ int medusa_workspace_size(const medusa_cfg* cfg, size_t* bytes) {
   int s = check_cfg(cfg);
   if (s != MEDUSA_OK) return s;
   if (!bytes) return MEDUSA_ERR_INVALID_ARG;
-  *bytes = align_up(heads_workspace(*cfg), 256) + align_up(attention_workspace(*cfg), 256);
+  *bytes = align_up(heads_workspace(*cfg), 256) + align_up(attention_workspace(*cfg), 256) + verify_workspace(*cfg);
   return MEDUSA_OK;
 }
 
@@ -75,7 +75,7 @@ int medusa_heads(const medusa_cfg* cfg, const void* h, const void* W, const void
   if (!h || !W || !U || !topk || !workspace) return MEDUSA_ERR_INVALID_ARG;
   if (!logits && cfg->mode == MEDUSA_REJECTION) return MEDUSA_ERR_INVALID_ARG;
   if (cfg->dtype == MEDUSA_BF16) {
-    if (cfg->d % 64 != 0) return MEDUSA_ERR_UNSUPPORTED;
+    if (cfg->d % 64 != 0 || cfg->B > 32) return MEDUSA_ERR_UNSUPPORTED;
     if (!aligned16(h) || !aligned16(W) || !aligned16(U)) return MEDUSA_ERR_INVALID_ARG;
   }
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MEDUSA_ERR_INVALID_ARG;
@@ -107,17 +107,20 @@ int medusa_tree_attention(const medusa_cfg* cfg, const void* Q, const void* Kc, 
 int medusa_verify(const medusa_cfg* cfg, const int32_t* tokens, const int32_t* parent, const int32_t* first_child,
                   const void* target_logits, const float* head_logits, const float* u_acc, const float* u_res,
                   int32_t* acc, int32_t* path, int32_t* out_tokens, int32_t* n_out, uint32_t* flags,
-                  medusa_stream_t stream) {
+                  void* workspace, medusa_stream_t stream) {
   int s = check_cfg(cfg);
   if (s != MEDUSA_OK) return s;
-  if (!tokens || !first_child || !target_logits || !acc || !path || !out_tokens || !n_out || !flags)
+  if (!tokens || !first_child || !target_logits || !acc || !path || !out_tokens || !n_out || !flags || !workspace)
     return MEDUSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MEDUSA_ERR_INVALID_ARG;
+  char* ws = static_cast<char*>(workspace) + align_up(heads_workspace(*cfg), 256) +
+             align_up(attention_workspace(*cfg), 256);
   if (cfg->mode == MEDUSA_REJECTION) {
     if (!head_logits || !u_acc || !u_res) return MEDUSA_ERR_INVALID_ARG;
     if (cfg->V > 32768) return MEDUSA_ERR_UNSUPPORTED;
   }
   return from_cuda(launch_verify(*cfg, tokens, parent, first_child, target_logits, head_logits, u_acc, u_res, acc,
-                                 path, out_tokens, n_out, flags, (cudaStream_t)stream));
+                                 path, out_tokens, n_out, flags, ws, (cudaStream_t)stream));
 }
 
 int medusa_kv_compact(const medusa_cfg* cfg, void* Kc, void* Vc, int32_t* L, const int32_t* acc, const int32_t* path,

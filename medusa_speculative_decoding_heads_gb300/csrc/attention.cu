@@ -60,6 +60,7 @@ AttnPlan plan_attention(const medusa_cfg& c) {
   int want = (int)((2L * 152 + ctas - 1) / ctas);
   int by_len = (Lmax + 255) / 256;
   p.nsplit = want < by_len ? want : by_len;
+  if (p.nsplit > 32) p.nsplit = 32;   // the merge gives one lane per split
   if (p.nsplit < 1) p.nsplit = 1;
   p.chunk = Lmax > 0 ? ((Lmax + p.nsplit - 1) / p.nsplit + tile - 1) / tile * tile : tile;
   const size_t rows = (size_t)c.B * p.nsplit * ts.N * c.Hq;
@@ -186,7 +187,8 @@ tree_attn_partial_kernel(const T* __restrict__ Q, const T* __restrict__ Kc, cons
   }
 }
 
-// O[b][i][h] = sum_s O_s 2^(m_s - M) / sum_s l_s 2^(m_s - M)
+// O[b][i][h] = sum_s O_s 2^(m_s - M) / sum_s l_s 2^(m_s - M); one warp per output
+// row, lane s holds split s's (m, l) (nsplit <= 32).
 template <typename T, int D>
 __global__ void tree_attn_merge_kernel(const float* __restrict__ o_part, const float* __restrict__ ml_part, int B,
                                        int N, int Hq, int nsplit, const int32_t* __restrict__ L, int L_cap,
@@ -200,23 +202,25 @@ __global__ void tree_attn_merge_kernel(const float* __restrict__ o_part, const f
   const int b = warp / (Hq * N);
   const int Lb = L[b];
   const bool valid = Lb >= 0 && Lb + N <= L_cap;
-  float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) {
-    size_t row = (((size_t)b * nsplit + s) * N + node) * Hq + h;
-    M = fmaxf(M, ml_part[2 * row]);
+  const size_t split_stride = (size_t)N * Hq;
+  const size_t row0 = ((size_t)b * nsplit * N + node) * Hq + h;   // split 0's partial row
+  float ms = -INFINITY, ls = 0.f;
+  if (lane < nsplit) {
+    ms = ml_part[2 * (row0 + lane * split_stride)];
+    ls = ml_part[2 * (row0 + lane * split_stride) + 1];
   }
-  float lsum = 0.f;
+  const float M = warp_max(ms);
+  const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+  const float lsum = warp_sum(ls * w);
   float acc[D / 32];
 #pragma unroll
   for (int j = 0; j < D / 32; ++j) acc[j] = 0.f;
+#pragma unroll 4
   for (int s = 0; s < nsplit; ++s) {
-    size_t row = (((size_t)b * nsplit + s) * N + node) * Hq + h;
-    float ms = ml_part[2 * row];
-    if (ms == -INFINITY) continue;
-    float w = exp2f(ms - M);
-    lsum += ml_part[2 * row + 1] * w;
+    const float ws = __shfl_sync(0xffffffffu, w, s);
+    const float* op = o_part + (row0 + s * split_stride) * D;
 #pragma unroll
-    for (int j = 0; j < D / 32; ++j) acc[j] += o_part[row * D + lane + 32 * j] * w;
+    for (int j = 0; j < D / 32; ++j) acc[j] += op[lane + 32 * j] * ws;
   }
   const size_t out = (((size_t)b * N + node) * Hq + h) * D;
 #pragma unroll
@@ -232,7 +236,8 @@ cudaError_t run(const medusa_cfg& c, const AttnPlan& p, const void* Q, const voi
   cudaError_t e;
   const int path = attention_path(c);
   if (path == kPathTc) {
-    e = launch_attention_tc(c, p.nsplit, p.chunk, Q, Kc, Vc, L, bits, o_part, ml_part, st);
+    e = launch_attention_tc(c, p.nsplit, p.chunk, Q, Kc, Vc, L, bits, o_part, ml_part, O, st);
+    if (e != cudaSuccess || p.nsplit == 1) return e;   // a single split writes O itself
   } else if (path == kPathMma) {
     e = launch_attention_mma(c, p.nsplit, p.chunk, Q, Kc, Vc, L, bits, o_part, ml_part, st);
   } else {

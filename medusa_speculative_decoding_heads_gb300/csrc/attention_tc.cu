@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const uint16_t* __restrict__ Q, const int32_t* __restrict__ L, const uint64_t* __restrict__ bits,
                     int N, int Hq, int Hkv, int L_cap, int chunk, float scale_log2, float* __restrict__ o_part,
-                    float* __restrict__ ml_part) {
+                    float* __restrict__ ml_part, uint16_t* __restrict__ O) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Qs = sm;
@@ -287,27 +287,54 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     xsum[hf][row] = l_run;
     tc::mbar_arrive(&sum_bar);
     tc::mbar_wait(&sum_bar, 0, err, 512);
-    const size_t orow = (((size_t)b * nsplit + split) * N + node) * Hq + qh;
+    const float l_tot = l_run + xsum[hf ^ 1][row];
+    if (nsplit == 1) {
+      // Single KV split: normalise and write O (bf16) directly, no merge pass.
+      const float inv = (have && l_tot > 0.f) ? 1.f / l_tot : 0.f;
+      uint16_t* op = O + (((size_t)b * N + node) * Hq + qh) * kD + col0;
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      uint32_t ov[32];
-      if (have) {
-        tc::tmem_ld32(tO + lane_base + col0 + c * 32, ov);
-        tc::tmem_wait_ld();
-      }
-      if (row_ok) {
-        float* op = o_part + orow * kD + col0 + c * 32;
+      for (int c = 0; c < 2; ++c) {
+        uint32_t ov[32];
+        if (have) {
+          tc::tmem_ld32(tO + lane_base + col0 + c * 32, ov);
+          tc::tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int x = 0; x < 32; x += 4)
-          *reinterpret_cast<float4*>(op + x) =
-              have ? make_float4(__uint_as_float(ov[x]), __uint_as_float(ov[x + 1]), __uint_as_float(ov[x + 2]),
-                                 __uint_as_float(ov[x + 3]))
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int x = 0; x < 32; ++x) ov[x] = 0u;
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int x = 0; x < 32; x += 8)
+            *reinterpret_cast<uint4*>(op + c * 32 + x) =
+                make_uint4(pack_bf16x2(__uint_as_float(ov[x]) * inv, __uint_as_float(ov[x + 1]) * inv),
+                           pack_bf16x2(__uint_as_float(ov[x + 2]) * inv, __uint_as_float(ov[x + 3]) * inv),
+                           pack_bf16x2(__uint_as_float(ov[x + 4]) * inv, __uint_as_float(ov[x + 5]) * inv),
+                           pack_bf16x2(__uint_as_float(ov[x + 6]) * inv, __uint_as_float(ov[x + 7]) * inv));
+        }
       }
-    }
-    if (row_ok && hf == 0) {
-      ml_part[2 * orow] = have ? m_run : -INFINITY;
-      ml_part[2 * orow + 1] = have ? l_run + xsum[1][row] : 0.f;
+    } else {
+      const size_t orow = (((size_t)b * nsplit + split) * N + node) * Hq + qh;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t ov[32];
+        if (have) {
+          tc::tmem_ld32(tO + lane_base + col0 + c * 32, ov);
+          tc::tmem_wait_ld();
+        }
+        if (row_ok) {
+          float* op = o_part + orow * kD + col0 + c * 32;
+#pragma unroll
+          for (int x = 0; x < 32; x += 4)
+            *reinterpret_cast<float4*>(op + x) =
+                have ? make_float4(__uint_as_float(ov[x]), __uint_as_float(ov[x + 1]), __uint_as_float(ov[x + 2]),
+                                   __uint_as_float(ov[x + 3]))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      if (row_ok && hf == 0) {
+        ml_part[2 * orow] = have ? m_run : -INFINITY;
+        ml_part[2 * orow + 1] = have ? l_tot : 0.f;
+      }
     }
   }
 
@@ -348,7 +375,7 @@ int attention_tc_mtiles(int NG) { return (NG + kRows - 1) / kRows; }
 
 cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, const void* Q, const void* Kc,
                                 const void* Vc, const int32_t* L, const uint64_t* bits, float* o_part, float* ml_part,
-                                cudaStream_t st) {
+                                void* O, cudaStream_t st) {
   const TreeShape ts = tree_shape(c);
   const uint64_t rows = (uint64_t)c.B * c.Hkv * c.L_cap;
   CUtensorMap tmK, tmV;
@@ -360,7 +387,8 @@ cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, cons
   const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)kD));
   dim3 grid(attention_tc_mtiles(ts.N * (c.Hq / c.Hkv)), c.Hkv * c.B, nsplit);
   tree_attn_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmK, tmV, static_cast<const uint16_t*>(Q), L, bits, ts.N, c.Hq,
-                                                     c.Hkv, c.L_cap, chunk, scale_log2, o_part, ml_part);
+                                                     c.Hkv, c.L_cap, chunk, scale_log2, o_part, ml_part,
+                                                     static_cast<uint16_t*>(O));
   note_launches(1);
   return cudaGetLastError();
 }

@@ -76,6 +76,16 @@ cudaError_t launch_heads(const medusa_cfg& c, const void* h, const void* W, cons
                          const void* U, float* logits, int32_t* topk, void* ws, cudaStream_t st);
 size_t heads_workspace(const medusa_cfg& c);
 
+// Tensor-core (tcgen05) heads path.
+struct HeadsTcPlan {
+  int NB, NCOL1, NCOL2, ksplit1;
+  size_t x1, x2, part1, total;
+};
+HeadsTcPlan plan_heads_tc(const medusa_cfg& c);
+bool heads_tc_supported(const medusa_cfg& c);
+cudaError_t launch_heads_tc(const medusa_cfg& c, const void* h, const void* W, const void* bias, const void* U,
+                            float* z, char* ws, cudaStream_t st);
+
 cudaError_t launch_tree_build(const medusa_cfg& c, const int32_t* root, const int32_t* topk,
                               const int32_t* L, int32_t* parent, int32_t* depth, int32_t* first_child,
                               uint8_t* mask, uint64_t* bits, int32_t* tokens, int32_t* pos,
@@ -88,7 +98,7 @@ int attention_mma_warps(int NG, int* row_blocks);
 int attention_tc_mtiles(int NG);
 cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, const void* Q, const void* Kc,
                                 const void* Vc, const int32_t* L, const uint64_t* bits, float* o_part, float* ml_part,
-                                cudaStream_t st);
+                                void* O, cudaStream_t st);
 cudaError_t launch_attention_mma(const medusa_cfg& c, int nsplit, int chunk, const void* Q, const void* Kc,
                                  const void* Vc, const int32_t* L, const uint64_t* bits, float* o_part, float* ml_part,
                                  cudaStream_t st);
@@ -96,7 +106,8 @@ cudaError_t launch_attention_mma(const medusa_cfg& c, int nsplit, int chunk, con
 cudaError_t launch_verify(const medusa_cfg& c, const int32_t* tokens, const int32_t* parent,
                           const int32_t* first_child, const void* tl, const float* hl,
                           const float* u_acc, const float* u_res, int32_t* acc, int32_t* path,
-                          int32_t* out_tokens, int32_t* n_out, uint32_t* flags, cudaStream_t st);
+                          int32_t* out_tokens, int32_t* n_out, uint32_t* flags, void* ws, cudaStream_t st);
+size_t verify_workspace(const medusa_cfg& c);
 
 cudaError_t launch_kv_compact(const medusa_cfg& c, void* Kc, void* Vc, int32_t* L, const int32_t* acc,
                               const int32_t* path, int32_t* kv_map, cudaStream_t st);

@@ -327,19 +327,76 @@ heads_f32_kernel(const float* __restrict__ A, int rows, int d, const float* __re
 }
 
 // ---------------------------------------------------------------- top-s per (b, k)
-// Order: value descending, index ascending.
+// Order: value descending, index ascending. Two kernels: many CTAs each reduce a
+// slice of a row to its top-s candidates, then one warp per row merges them.
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-constexpr int kTopThreads = 1024;
+constexpr int kTopThreads = 256;
 
+// Warp-wide best of (v, i) pairs; returns the winner's pair and lane in all lanes.
+__device__ __forceinline__ void warp_best(float& v, int& i, int& who) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    const int ow = __shfl_xor_sync(0xffffffffu, who, o);
+    if (better(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+      who = ow;
+    }
+  }
+}
+
+// Pops the s best of the lanes' sorted lists (lv/li, kMaxS deep) in order.
+__device__ __forceinline__ void warp_top_s(float* lv, int* li, int s, float* ov, int* oi) {
+  const int lane = threadIdx.x & 31;
+  for (int r = 0; r < s; ++r) {
+    float v = lv[0];
+    int i = li[0];
+    int who = lane;
+    warp_best(v, i, who);
+    ov[r] = v;
+    oi[r] = i;
+    if (lane == who) {
+#pragma unroll
+      for (int k = 0; k < kMaxS - 1; ++k) {
+        lv[k] = lv[k + 1];
+        li[k] = li[k + 1];
+      }
+      lv[kMaxS - 1] = -INFINITY;
+      li[kMaxS - 1] = 0x7fffffff;
+    }
+  }
+}
+
+__device__ __forceinline__ void list_insert(float* lv, int* li, float x, int v) {
+  if (!better(x, v, lv[kMaxS - 1], li[kMaxS - 1])) return;
+  float cv = x;
+  int ci = v;
+#pragma unroll
+  for (int k = 0; k < kMaxS; ++k) {
+    if (better(cv, ci, lv[k], li[k])) {
+      const float tv = lv[k];
+      const int ti = li[k];
+      lv[k] = cv;
+      li[k] = ci;
+      cv = tv;
+      ci = ti;
+    }
+  }
+}
+
+// grid (P, K, B): slice p of row (b, k) -> s candidates at cand[((b*K + k)*P + p)*s_max + r].
 __global__ void __launch_bounds__(kTopThreads)
-topk_kernel(const float* __restrict__ z, int V, TreeShape ts, int32_t* __restrict__ topk) {
-  const int k = blockIdx.x, b = blockIdx.y;
-  const int K = ts.K, s_max = ts.s_max;
-  const int s = ts.s[k + 1];
+topk_partial_kernel(const float* __restrict__ z, int V, TreeShape ts, int chunk, float* __restrict__ cv,
+                    int* __restrict__ ci) {
+  const int p = blockIdx.x, k = blockIdx.y, b = blockIdx.z, P = gridDim.x;
+  const int K = ts.K, s = ts.s[k + 1], s_max = ts.s_max;
   const float* row = z + ((size_t)b * K + k) * V;
+  const int v0 = p * chunk, v1 = min(V, v0 + chunk);
   float lv[kMaxS];
   int li[kMaxS];
 #pragma unroll
@@ -347,92 +404,71 @@ topk_kernel(const float* __restrict__ z, int V, TreeShape ts, int32_t* __restric
     lv[i] = -INFINITY;
     li[i] = 0x7fffffff;
   }
-  for (int v = threadIdx.x; v < V; v += kTopThreads) {
-    float x = row[v];
-    if (!better(x, v, lv[kMaxS - 1], li[kMaxS - 1])) continue;
-    // insert into the sorted list
-    float cv = x;
-    int ci = v;
+  for (int v = v0 + threadIdx.x; v < v1; v += kTopThreads) list_insert(lv, li, row[v], v);
+  __shared__ float wv[kTopThreads / 32][kMaxS];
+  __shared__ int wi[kTopThreads / 32][kMaxS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float tv[kMaxS];
+  int ti[kMaxS];
+  warp_top_s(lv, li, s, tv, ti);
+  if (lane == 0)
+    for (int r = 0; r < s; ++r) {
+      wv[warp][r] = tv[r];
+      wi[warp][r] = ti[r];
+    }
+  __syncthreads();
+  if (warp == 0) {
+    // lane w < 8 holds warp w's sorted list
 #pragma unroll
     for (int i = 0; i < kMaxS; ++i) {
-      if (better(cv, ci, lv[i], li[i])) {
-        float tv = lv[i];
-        int ti = li[i];
-        lv[i] = cv;
-        li[i] = ci;
-        cv = tv;
-        ci = ti;
-      }
+      const bool have = lane < kTopThreads / 32 && i < s;
+      lv[i] = have ? wv[lane][i] : -INFINITY;
+      li[i] = have ? wi[lane][i] : 0x7fffffff;
     }
-  }
-  __shared__ float wv[kTopThreads / 32];
-  __shared__ int wi[kTopThreads / 32];
-  __shared__ int wl[kTopThreads / 32];
-  __shared__ int win_lane;
-  int head = 0;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = 0; r < s; ++r) {
-    float cv = head < kMaxS ? lv[0] : -INFINITY;
-    int ci = head < kMaxS ? li[0] : 0x7fffffff;
-    int who = threadIdx.x;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, cv, o);
-      int oi = __shfl_xor_sync(0xffffffffu, ci, o);
-      int ow = __shfl_xor_sync(0xffffffffu, who, o);
-      if (better(ov, oi, cv, ci)) {
-        cv = ov;
-        ci = oi;
-        who = ow;
-      }
-    }
+    warp_top_s(lv, li, s, tv, ti);
     if (lane == 0) {
-      wv[warp] = cv;
-      wi[warp] = ci;
-      wl[warp] = who;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      cv = lane < kTopThreads / 32 ? wv[lane] : -INFINITY;
-      ci = lane < kTopThreads / 32 ? wi[lane] : 0x7fffffff;
-      who = lane < kTopThreads / 32 ? wl[lane] : -1;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, cv, o);
-        int oi = __shfl_xor_sync(0xffffffffu, ci, o);
-        int ow = __shfl_xor_sync(0xffffffffu, who, o);
-        if (better(ov, oi, cv, ci)) {
-          cv = ov;
-          ci = oi;
-          who = ow;
-        }
-      }
-      if (lane == 0) {
-        win_lane = who;
-        topk[((size_t)b * K + k) * s_max + r] = ci;
+      const size_t o = (((size_t)b * K + k) * P + p) * s_max;
+      for (int r = 0; r < s; ++r) {
+        cv[o + r] = tv[r];
+        ci[o + r] = ti[r];
       }
     }
-    __syncthreads();
-    if (threadIdx.x == win_lane) {
-      // pop the head of this thread's list
-#pragma unroll
-      for (int i = 0; i < kMaxS - 1; ++i) {
-        lv[i] = lv[i + 1];
-        li[i] = li[i + 1];
-      }
-      lv[kMaxS - 1] = -INFINITY;
-      li[kMaxS - 1] = 0x7fffffff;
-      ++head;
-    }
-    __syncthreads();
   }
-  for (int r = s + threadIdx.x; r < s_max; r += kTopThreads) topk[((size_t)b * K + k) * s_max + r] = -1;
+}
+
+// grid (K, B), one warp: merge P slices' candidates into topk[b][k][:].
+__global__ void topk_merge_kernel(const float* __restrict__ cv, const int* __restrict__ ci, int P, TreeShape ts,
+                                  int32_t* __restrict__ topk) {
+  const int k = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
+  const int K = ts.K, s = ts.s[k + 1], s_max = ts.s_max;
+  float lv[kMaxS];
+  int li[kMaxS];
+#pragma unroll
+  for (int i = 0; i < kMaxS; ++i) {
+    lv[i] = -INFINITY;
+    li[i] = 0x7fffffff;
+  }
+  const size_t base = ((size_t)b * K + k) * P * s_max;
+  for (int p = lane; p < P; p += 32)
+    for (int r = 0; r < s; ++r) list_insert(lv, li, cv[base + (size_t)p * s_max + r], ci[base + (size_t)p * s_max + r]);
+  float tv[kMaxS];
+  int ti[kMaxS];
+  warp_top_s(lv, li, s, tv, ti);
+  if (lane == 0)
+    for (int r = 0; r < s_max; ++r) topk[((size_t)b * K + k) * s_max + r] = r < s ? ti[r] : -1;
+}
+
+int topk_slices(const medusa_cfg& c) {
+  int P = (4 * 152 + c.K * c.B - 1) / (c.K * c.B);
+  P = P < 1 ? 1 : (P > 64 ? 64 : P);
+  const int max_by_len = (c.V + 255) / 256;
+  return P < max_by_len ? P : (max_by_len < 1 ? 1 : max_by_len);
 }
 
 struct HeadsPlan {
   int NT;          // 8-wide batch tiles (bf16 path)
   int ksplit1;     // split of d for the d x d layer
-  size_t xp1, xp2, part1, zbuf, total;   // byte offsets / sizes
+  size_t xp1, xp2, part1, zbuf, cand, tc, total;   // byte offsets / sizes
 };
 
 HeadsPlan plan_heads(const medusa_cfg& c) {
@@ -451,7 +487,9 @@ HeadsPlan plan_heads(const medusa_cfg& c) {
     off = align_up(off + bytes, 256);
     return o;
   };
-  if (c.dtype == MEDUSA_BF16) {
+  if (heads_tc_supported(c)) {
+    p.xp1 = p.xp2 = p.part1 = take(0);
+  } else if (c.dtype == MEDUSA_BF16) {
     p.xp1 = take((size_t)nchunks * p.NT * 1024);
     p.xp2 = take(K * nchunks * p.NT * 2048);
     p.part1 = take((size_t)p.ksplit1 * B * K * d * 4);
@@ -461,6 +499,8 @@ HeadsPlan plan_heads(const medusa_cfg& c) {
     p.part1 = take(0);
   }
   p.zbuf = take(B * K * V * 4);
+  p.cand = take((size_t)B * K * topk_slices(c) * kMaxS * 8);
+  if (heads_tc_supported(c)) p.tc = take(plan_heads_tc(c).total);
   p.total = off;
   return p;
 }
@@ -476,7 +516,10 @@ cudaError_t launch_heads(const medusa_cfg& c, const void* h, const void* W, cons
   const int B = c.B, d = c.d, V = c.V, K = c.K;
   float* z = logits ? logits : reinterpret_cast<float*>(base + p.zbuf);
 
-  if (c.dtype == MEDUSA_BF16) {
+  if (heads_tc_supported(c)) {
+    cudaError_t e = launch_heads_tc(c, h, W, bias, U, z, base + p.tc, st);
+    if (e != cudaSuccess) return e;
+  } else if (c.dtype == MEDUSA_BF16) {
     uint16_t* xp1 = reinterpret_cast<uint16_t*>(base + p.xp1);
     uint16_t* xp2 = reinterpret_cast<uint16_t*>(base + p.xp2);
     float* part1 = reinterpret_cast<float*>(base + p.part1);
@@ -512,7 +555,14 @@ cudaError_t launch_heads(const medusa_cfg& c, const void* h, const void* W, cons
                                                 K, z, nullptr, nullptr);
     note_launches(1);
   }
-  topk_kernel<<<dim3(K, B), kTopThreads, 0, st>>>(z, V, tree_shape(c), topk);
+  const TreeShape ts = tree_shape(c);
+  const int P = topk_slices(c);
+  const int chunk = (V + P - 1) / P;
+  float* cv = reinterpret_cast<float*>(base + p.cand);
+  int* ci = reinterpret_cast<int*>(cv + (size_t)B * K * P * kMaxS);
+  topk_partial_kernel<<<dim3(P, K, B), kTopThreads, 0, st>>>(z, V, ts, chunk, cv, ci);
+  note_launches(1);
+  topk_merge_kernel<<<dim3(K, B), 32, 0, st>>>(cv, ci, P, ts, topk);
   note_launches(1);
   return cudaGetLastError();
 }

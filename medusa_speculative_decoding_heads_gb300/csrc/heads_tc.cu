@@ -1,0 +1,307 @@
+// Medusa heads on tcgen05 tensor cores with TMA-fed weight streaming.
+//
+// "Medusa 심층 아키텍처" (techknowgenie), section "Medusa의 핵심 철학", equations
+// h_t^(k) = SiLU(h_t W_res^(k)) + h_t and p_k = softmax(h_t^(k) W_head^(k)).
+//
+// Both projections are weight-streaming GEMVs: every weight byte is read once
+// and meets all B vectors of the batch. Swap-AB: 128 weight rows are the MMA's
+// M dimension (A operand, K-major, straight from the row-major weights), the
+// batch vectors are the N dimension (B operand). The vocab projection consumes
+// the f32 residual as bf16 hi and lo vectors, i.e. N = 2 * NB columns; the two
+// columns of a sequence are added in the epilogue.
+//
+// Persistent CTAs (one per SM) walk a static list of work units (head, 128-row
+// tile, k-split); 6 warps:
+//   warp 4  TMA producer: 64-wide k chunks of the weight tile and of the vector
+//           tile into a deep shared-memory ring (128-byte swizzle).
+//   warp 5  MMA issuer: four K=16 MMAs per chunk into one of two TMEM
+//           accumulators; commits free ring slots and completed units.
+//   warps 0-3  epilogue: thread i = weight row i = TMEM lane i; adds the hi/lo
+//           columns and writes f32 outputs (coalesced across the warp).
+// All mbarrier waits are bounded (see tc_common.cuh).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "tc_common.cuh"
+
+namespace medusa {
+
+__device__ uint32_t g_heads_tc_error = 0;
+
+namespace {
+
+constexpr int kRowsTile = 128;
+constexpr int kChunkK = 64;
+constexpr int kATile = kRowsTile * 128;     // 16 KB: 128 rows x 64 bf16
+constexpr int kSmemBudget = 200 * 1024;
+constexpr uint32_t kAccCols = 64;           // columns per TMEM accumulator (N <= 64)
+
+template <int NCOL>
+struct HeadsGeom {
+  static constexpr int kXTile = NCOL * 128;
+  static constexpr int kStage = kATile + kXTile;
+  static constexpr int kStages = (kSmemBudget / kStage) > 12 ? 12 : (kSmemBudget / kStage);
+  static constexpr int kSmem = kStages * kStage + 1024;
+};
+
+// out[ks][b][g][r] = sum_k A[g*rows + r][k] * X[g*x_rows + col(b)][k] over the
+// unit's k range; col(b) = b (+ NB for the lo part when HILO).
+template <int NCOL, bool HILO>
+__global__ void __launch_bounds__(192, 1)
+heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmX, int rows, int G,
+                int x_rows, int nchunks, int nk, int ksplit, int B, float* __restrict__ out,
+                size_t out_split_stride) {
+  using Geo = HeadsGeom<NCOL>;
+  constexpr int S = Geo::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* As = sm;                       // [S][16 KB]
+  uint8_t* Xs = sm + S * kATile;          // [S][NCOL * 128]
+  __shared__ __align__(8) uint64_t full[S], empty[S], acc_full[2], acc_empty[2];
+  __shared__ uint32_t tmem_slot;
+  uint32_t* err = &g_heads_tc_error;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles = (rows + kRowsTile - 1) / kRowsTile;
+  const int nunits = G * tiles * ksplit;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&acc_full[a], 1);
+      tc::mbar_init(&acc_empty[a], 128);
+    }
+    tc::mbar_fence_init();
+  }
+  if (warp == 4) tc::tmem_alloc(&tmem_slot, 2 * kAccCols);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const int ks = u % ksplit, t = (u / ksplit) % tiles, g = u / (ksplit * tiles);
+        const int c0 = ks * nk, c1 = min(nchunks, c0 + nk);
+        for (int c = c0; c < c1; ++c, ++it) {
+          const int s = it % S;
+          if (it >= S && !tc::mbar_wait(&empty[s], ((it / S) - 1) & 1, err, 1)) {
+            ok = false;
+            break;
+          }
+          tc::mbar_arrive_expect(&full[s], kATile + Geo::kXTile);
+          tc::tma_load_2d(As + s * kATile, &tmA, c * kChunkK, g * rows + t * kRowsTile, &full[s]);
+          tc::tma_load_2d(Xs + s * Geo::kXTile, &tmX, c * kChunkK, g * x_rows, &full[s]);
+        }
+      }
+      // Drain the loads still in flight before the CTA can exit.
+      for (int j = it > S ? it - S : 0; j < it; ++j) tc::mbar_wait(&full[j % S], (j / S) & 1, err, 2);
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kRowsTile, NCOL, 0, 0);
+      int it = 0, ui = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++ui) {
+        const int ks = u % ksplit;
+        const int c0 = ks * nk, c1 = min(nchunks, c0 + nk);
+        const int a = ui & 1;
+        if (ui >= 2 && !tc::mbar_wait(&acc_empty[a], ((ui >> 1) - 1) & 1, err, 4)) break;
+        tc::fence_after();
+        const uint32_t dacc = tmem + a * kAccCols;
+        for (int c = c0; c < c1; ++c, ++it) {
+          const int s = it % S;
+          if (!tc::mbar_wait(&full[s], (it / S) & 1, err, 8)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after();
+          const uint32_t aa = tc::saddr(As + s * kATile), xa = tc::saddr(Xs + s * Geo::kXTile);
+#pragma unroll
+          for (int kk = 0; kk < kChunkK / 16; ++kk)
+            tc::mma_bf16(dacc, tc::sw128_desc(aa + kk * 32, 16, 1024), tc::sw128_desc(xa + kk * 32, 16, 1024), idesc,
+                         (c > c0 || kk > 0) ? 1 : 0);
+          tc::commit(&empty[s]);
+        }
+        tc::commit(&acc_full[a]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const int i = threadIdx.x;
+    int ui = 0;
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++ui) {
+      const int ks = u % ksplit, t = (u / ksplit) % tiles, g = u / (ksplit * tiles);
+      const int a = ui & 1;
+      const bool ok = tc::mbar_wait(&acc_full[a], (ui >> 1) & 1, err, 16);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc::fence_after();
+      uint32_t v[64];
+      tc::tmem_ld32(tmem + a * kAccCols + lane_base, v);
+      if (NCOL > 32) tc::tmem_ld32(tmem + a * kAccCols + lane_base + 32, v + 32);
+      tc::tmem_wait_ld();
+      tc::fence_before();
+      tc::mbar_arrive(&acc_empty[a]);
+      const int r = t * kRowsTile + i;
+      if (r < rows) {
+        float* o = out + (size_t)ks * out_split_stride + (size_t)g * rows + r;
+        const size_t bstride = (size_t)G * rows;
+        constexpr int kCols = HILO ? NCOL / 2 : NCOL;   // batch columns (lo part follows when HILO)
+#pragma unroll
+        for (int b = 0; b < kCols; ++b) {
+          if (b < B) {
+            float x = __uint_as_float(v[b]);
+            if (HILO) x += __uint_as_float(v[kCols + b]);
+            o[(size_t)b * bstride] = x;
+          }
+        }
+      }
+    }
+  }
+
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc::fence_after();
+    tc::tmem_dealloc(tmem, 2 * kAccCols);
+  }
+}
+
+// X1[n][i] = h[n][i] (bf16) for n < B, zero rows up to NCOL1.
+__global__ void pack_h_tc_kernel(const uint16_t* __restrict__ h, uint16_t* __restrict__ X1, int B, int NCOL1, int d) {
+  const size_t total = (size_t)NCOL1 * d / 8;
+  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < total; v += (size_t)gridDim.x * blockDim.x) {
+    const int n = (int)(v * 8 / d);
+    const int i = (int)(v * 8 % d);
+    uint4 x = make_uint4(0, 0, 0, 0);
+    if (n < B) x = *reinterpret_cast<const uint4*>(h + (size_t)n * d + i);
+    *reinterpret_cast<uint4*>(X1 + v * 8) = x;
+  }
+}
+
+// r = h + SiLU(sum_splits pre + bias); X2[k][n][o] = bf16(r), X2[k][NB+n][o] = bf16(r - bf16(r)).
+__global__ void residual_pack_tc_kernel(const float* __restrict__ part, int ksplit, const uint16_t* __restrict__ h,
+                                        const uint16_t* __restrict__ bias, uint16_t* __restrict__ X2, int B, int NB,
+                                        int K, int d) {
+  const size_t total = (size_t)K * NB * d;
+  const size_t split_stride = (size_t)B * K * d;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
+    const int o = (int)(e % d);
+    const int n = (int)((e / d) % NB);
+    const int k = (int)(e / ((size_t)d * NB));
+    uint16_t hi = 0, lo = 0;
+    if (n < B) {
+      float pre = 0.f;
+      for (int s = 0; s < ksplit; ++s) pre += part[s * split_stride + ((size_t)n * K + k) * d + o];
+      if (bias) pre += bf16_to_f32(bias[(size_t)k * d + o]);
+      const float r = bf16_to_f32(h[(size_t)n * d + o]) + pre / (1.f + expf(-pre));
+      hi = f32_to_bf16(r);
+      lo = f32_to_bf16(r - bf16_to_f32(hi));
+    }
+    uint16_t* xk = X2 + (size_t)k * 2 * NB * d;
+    xk[(size_t)n * d + o] = hi;
+    xk[(size_t)(NB + n) * d + o] = lo;
+  }
+}
+
+template <int NCOL, bool HILO>
+cudaError_t run_gemv(const CUtensorMap& tmA, const CUtensorMap& tmX, int rows, int G, int x_rows, int nchunks, int ks,
+                     int B, float* out, size_t out_split_stride, int num_sms, cudaStream_t st) {
+  using Geo = HeadsGeom<NCOL>;
+  const int nk = (nchunks + ks - 1) / ks;   // ks comes from plan_heads_tc: every split has >= 1 chunk
+  const int tiles = (rows + kRowsTile - 1) / kRowsTile;
+  const int nunits = G * tiles * ks;
+  cudaError_t e = cudaFuncSetAttribute(heads_tc_kernel<NCOL, HILO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Geo::kSmem);
+  if (e != cudaSuccess) return e;
+  const int grid = nunits < num_sms ? nunits : num_sms;
+  heads_tc_kernel<NCOL, HILO><<<grid, 192, Geo::kSmem, st>>>(tmA, tmX, rows, G, x_rows, nchunks, nk, ks, B, out,
+                                                              out_split_stride);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+// Workspace layout of the tensor-core heads path.
+HeadsTcPlan plan_heads_tc(const medusa_cfg& c) {
+  HeadsTcPlan p{};
+  p.NB = c.B <= 8 ? 8 : (c.B + 7) / 8 * 8;               // batch columns per part (hi or lo)
+  p.NCOL1 = c.B <= 16 ? 16 : 32;                          // d x d layer: h only
+  p.NCOL2 = 2 * p.NB;                                     // vocab projection: hi and lo
+  const int nchunks = c.d / kChunkK;
+  const int units1 = c.K * ((c.d + kRowsTile - 1) / kRowsTile);
+  int ks = (4 * 148 + units1 - 1) / units1;
+  ks = ks < 1 ? 1 : (ks > nchunks ? nchunks : ks);
+  const int nk = (nchunks + ks - 1) / ks;
+  p.ksplit1 = (nchunks + nk - 1) / nk;                    // no empty split
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  p.x1 = take((size_t)p.NCOL1 * c.d * 2);
+  p.x2 = take((size_t)c.K * p.NCOL2 * c.d * 2);
+  p.part1 = take((size_t)p.ksplit1 * c.B * c.K * c.d * 4);
+  p.total = off;
+  return p;
+}
+
+bool heads_tc_supported(const medusa_cfg& c) { return c.dtype == MEDUSA_BF16 && c.B <= 32 && c.d % 64 == 0; }
+
+cudaError_t launch_heads_tc(const medusa_cfg& c, const void* h, const void* W, const void* bias, const void* U,
+                            float* z, char* ws, cudaStream_t st) {
+  const HeadsTcPlan p = plan_heads_tc(c);
+  uint16_t* x1 = reinterpret_cast<uint16_t*>(ws + p.x1);
+  uint16_t* x2 = reinterpret_cast<uint16_t*>(ws + p.x2);
+  float* part1 = reinterpret_cast<float*>(ws + p.part1);
+  const int B = c.B, d = c.d, V = c.V, K = c.K;
+  const int nchunks = d / kChunkK;
+  CUtensorMap tmW, tmX1, tmU, tmX2;
+  if (!encode_tmap_2d_bf16(&tmW, W, (uint64_t)K * d, d, (uint64_t)d * 2, kChunkK, kRowsTile) ||
+      !encode_tmap_2d_bf16(&tmX1, x1, p.NCOL1, d, (uint64_t)d * 2, kChunkK, p.NCOL1) ||
+      !encode_tmap_2d_bf16(&tmU, U, (uint64_t)K * V, d, (uint64_t)d * 2, kChunkK, kRowsTile) ||
+      !encode_tmap_2d_bf16(&tmX2, x2, (uint64_t)K * p.NCOL2, d, (uint64_t)d * 2, kChunkK, p.NCOL2))
+    return cudaErrorInvalidValue;
+  const int sms = sm_count();
+
+  pack_h_tc_kernel<<<64, 256, 0, st>>>(static_cast<const uint16_t*>(h), x1, B, p.NCOL1, d);
+  note_launches(1);
+  cudaError_t e = p.NCOL1 == 16
+                      ? run_gemv<16, false>(tmW, tmX1, d, K, 0, nchunks, p.ksplit1, B, part1, (size_t)B * K * d, sms, st)
+                      : run_gemv<32, false>(tmW, tmX1, d, K, 0, nchunks, p.ksplit1, B, part1, (size_t)B * K * d, sms, st);
+  if (e != cudaSuccess) return e;
+  residual_pack_tc_kernel<<<512, 256, 0, st>>>(part1, p.ksplit1, static_cast<const uint16_t*>(h),
+                                               static_cast<const uint16_t*>(bias), x2, B, p.NB, K, d);
+  note_launches(1);
+  switch (p.NCOL2) {
+    case 16: return run_gemv<16, true>(tmU, tmX2, V, K, p.NCOL2, nchunks, 1, B, z, 0, sms, st);
+    case 32: return run_gemv<32, true>(tmU, tmX2, V, K, p.NCOL2, nchunks, 1, B, z, 0, sms, st);
+    case 48: return run_gemv<48, true>(tmU, tmX2, V, K, p.NCOL2, nchunks, 1, B, z, 0, sms, st);
+    default: return run_gemv<64, true>(tmU, tmX2, V, K, p.NCOL2, nchunks, 1, B, z, 0, sms, st);
+  }
+}
+
+}  // namespace medusa

@@ -35,31 +35,39 @@ tree_build_kernel(TreeShape ts, int B, int L_cap, const int32_t* __restrict__ ro
                   const int32_t* __restrict__ L, int32_t* __restrict__ parent, int32_t* __restrict__ depth,
                   int32_t* __restrict__ first_child, uint8_t* __restrict__ mask, uint64_t* __restrict__ bits,
                   int32_t* __restrict__ tokens, int32_t* __restrict__ pos, uint32_t* __restrict__ flags) {
+  __shared__ uint64_t sb[kMaxN][2];
   const int b = blockIdx.x;
   const int n = threadIdx.x;
   const int N = ts.N;
   const int Lb = L[b];
   if (n == 0 && flags) flags[b] = (Lb < 0 || Lb + N > L_cap) ? MEDUSA_FLAG_CAPACITY : 0u;
-  if (n >= N) return;
-  const int d = node_depth(ts, n);
+  const int d = n < N ? node_depth(ts, n) : 0;
   const int t = n - ts.off[d];
-  const int rank = d > 0 ? t % ts.s[d] : 0;
-  tokens[(size_t)b * N + n] = d == 0 ? root[b] : topk[((size_t)b * ts.K + (d - 1)) * ts.s_max + rank];
-  pos[(size_t)b * N + n] = Lb + d;
-  if (b != 0) return;
-  parent[n] = d > 0 ? ts.off[d - 1] + t / ts.s[d] : -1;
-  depth[n] = d;
-  first_child[n] = d < ts.K ? ts.off[d + 1] + t * ts.s[d + 1] : -1;
-  uint64_t w0 = 0, w1 = 0;
-  for (int j = n; j >= 0; j = node_parent(ts, j)) {
-    if (j < 64) w0 |= 1ull << j;
-    else w1 |= 1ull << (j - 64);
+  if (n < N) {
+    const int rank = d > 0 ? t % ts.s[d] : 0;
+    tokens[(size_t)b * N + n] = d == 0 ? root[b] : topk[((size_t)b * ts.K + (d - 1)) * ts.s_max + rank];
+    pos[(size_t)b * N + n] = Lb + d;
   }
-  bits[2 * n] = w0;
-  bits[2 * n + 1] = w1;
-  for (int j = 0; j < N; ++j) {
-    uint64_t w = j < 64 ? w0 : w1;
-    mask[(size_t)n * N + j] = uint8_t((w >> (j & 63)) & 1ull);
+  if (b != 0) return;   // the tree arrays are the same for every sequence: block 0 writes them
+  if (n < N) {
+    parent[n] = d > 0 ? ts.off[d - 1] + t / ts.s[d] : -1;
+    depth[n] = d;
+    first_child[n] = d < ts.K ? ts.off[d + 1] + t * ts.s[d + 1] : -1;
+    uint64_t w0 = 0, w1 = 0;
+    for (int j = n; j >= 0; j = node_parent(ts, j)) {
+      if (j < 64) w0 |= 1ull << j;
+      else w1 |= 1ull << (j - 64);
+    }
+    sb[n][0] = w0;
+    sb[n][1] = w1;
+    bits[2 * n] = w0;
+    bits[2 * n + 1] = w1;
+  }
+  __syncthreads();
+  // mask row-major N x N, written with consecutive threads on consecutive bytes
+  for (int e = n; e < N * N; e += kMaxN) {
+    const int i = e / N, j = e - i * N;
+    mask[e] = uint8_t((sb[i][j >> 6] >> (j & 63)) & 1ull);
   }
 }
 

@@ -73,7 +73,7 @@ class DeviceStep:
         mb.verify(self.cfg, self.tokens if tokens is None else tokens, self.parent, self.first_child,
                   target_logits, (self.logits if head_logits is None else head_logits) if rs else None,
                   u_acc if rs else None, u_res if rs else None, self.acc, self.path, self.out_tokens, self.n_out,
-                  self.flags, self.stream)
+                  self.flags, self.workspace, self.stream)
 
     def kv_compact(self, Kc, Vc, L):
         mb.kv_compact(self.cfg, Kc, Vc, L, self.acc, self.path, self.kv_map, self.stream)

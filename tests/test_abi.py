@@ -88,7 +88,7 @@ def test_null_pointers_are_rejected(lib):
     assert lib.medusa_heads(ctypes.byref(cfg), None, None, None, None, None, None, None, None) == -1
     assert lib.medusa_tree_build(ctypes.byref(cfg), *([None] * 12)) == -1
     assert lib.medusa_tree_attention(ctypes.byref(cfg), *([None] * 8)) == -1
-    assert lib.medusa_verify(ctypes.byref(cfg), *([None] * 13)) == -1
+    assert lib.medusa_verify(ctypes.byref(cfg), *([None] * 14)) == -1
     assert lib.medusa_kv_compact(ctypes.byref(cfg), *([None] * 7)) == -1
     rs = _cfg(mode=configs.REJECTION, temperature=0.0)
     assert lib.medusa_workspace_size(ctypes.byref(rs), ctypes.byref(ctypes.c_size_t())) == -1
@@ -99,4 +99,4 @@ def test_rejection_mode_needs_logits_and_uniforms(lib):
     fake = ctypes.c_void_p(256)   # never dereferenced: validation fails first
     assert lib.medusa_heads(ctypes.byref(cfg), fake, fake, None, fake, None, fake, fake, None) == -1
     assert lib.medusa_verify(ctypes.byref(cfg), fake, fake, fake, fake, None, None, None, fake, fake, fake, fake,
-                             fake, None) == -1
+                             fake, fake, None) == -1
