@@ -8,16 +8,18 @@
 // One CTA = 128 query rows (tree nodes x query heads of one KV head) against one
 // KV range of one sequence; 10 warps:
 //   warp 8  TMA producer: K and V tiles of 128 keys (two 64-column boxes each,
-//           128-byte swizzle) into a 2-stage ring; allocates / frees TMEM.
-//   warp 9  MMA issuer (one thread): S_j = Q K_j^T into TMEM (double buffer),
-//           then O += P_j V_j (V as an MN-major operand), O in TMEM.
+//           128-byte swizzle) into a 3-stage ring; allocates / frees TMEM.
+//   warp 9  MMA issuer (one thread): S_j = Q K_j^T into TMEM (double buffer,
+//           Q itself held in TMEM), then O += P_j V_j with P_j read from TMEM
+//           and V as an MN-major shared-memory operand; O stays in TMEM.
+//           Shared memory holds only the K/V ring, so three 64 KB stages fit.
 //   warps 0-7  softmax: query row i = TMEM lane i is shared by warps w and w+4
 //           (64 columns each; the row maximum is combined through shared
 //           memory); each thread reads its half of S_j,
 //           applies the prefix range or the ancestor bitmask, keeps the running
 //           max / exp-sum (the max moves, and O is rescaled, only on a jump of
-//           more than 2^8), writes P_j (bf16) to shared memory in the swizzled
-//           K-major layout the MMA reads.
+//           more than 2^8), writes P_j (bf16 pairs) over its S slot in TMEM;
+//           tile j+1's softmax never waits for PV_j unless O must be rescaled.
 // Every mbarrier wait is bounded (a few seconds of clock cycles); on expiry the
 // thread records a code in a device error word and leaves its loop.
 #include <cuda.h>
@@ -42,7 +44,8 @@ constexpr int kRows = 128;
 constexpr int kD = 128;
 constexpr int kHalf = kRows * 128;          // bytes of one 64-column swizzled half tile (16 KB)
 constexpr int kTile = 2 * kHalf;            // 32 KB: a 128 x 128 bf16 tile
-constexpr int kSmemBytes = 6 * kTile + 1024;
+constexpr int kStages = 3;                  // K/V ring depth
+constexpr int kSmemBytes = 2 * kStages * kTile + 1024;
 constexpr uint32_t kTmemCols = 512;
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -62,6 +65,10 @@ constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr int kMmaWarp = kSoftmaxWarps + 1;
 constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
 
+// TMEM columns: S double buffer (P_j overwrites the first 64 columns of its S
+// slot once both halves of the row have read S_j), O, and Q (bf16 pairs).
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColQ = 384;
+
 __global__ void __launch_bounds__(kThreads, 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const uint16_t* __restrict__ Q, const int32_t* __restrict__ L, const uint64_t* __restrict__ bits,
@@ -69,11 +76,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     float* __restrict__ ml_part, uint16_t* __restrict__ O) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* Qs = sm;
-  uint8_t* Ps = sm + kTile;
-  uint8_t* Ks = sm + 2 * kTile;   // [2 stages]
-  uint8_t* Vs = sm + 4 * kTile;   // [2 stages]
-  __shared__ __align__(8) uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done;
+  uint8_t* Ks = sm;                        // [kStages]
+  uint8_t* Vs = sm + kStages * kTile;      // [kStages]
+  __shared__ __align__(8) uint64_t kv_full[kStages], kv_empty[kStages], s_full[2], p_full[2], p_free[2];
   __shared__ __align__(8) uint64_t x_bar[2], sum_bar;   // row-max / row-sum exchange between column halves
   __shared__ uint32_t tmem_slot;
   __shared__ float xmax[2][2][kRows];   // [tile parity][column half][row]: partial row maxima
@@ -92,20 +97,26 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   const int ntiles = ptiles + ((valid && split == nsplit - 1) ? 1 : 0);   // N <= 128: one tree tile
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&kv_full[s], 1);
       tc::mbar_init(&kv_empty[s], 1);
-      tc::mbar_init(&s_full[s], 1);
-      tc::mbar_init(&s_free[s], kSoftmaxThreads);
     }
-    tc::mbar_init(&p_full, kSoftmaxThreads);
-    tc::mbar_init(&o_done, 1);
-    tc::mbar_init(&x_bar[0], kSoftmaxThreads);
-    tc::mbar_init(&x_bar[1], kSoftmaxThreads);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&s_full[s], 1);
+      tc::mbar_init(&p_full[s], kSoftmaxThreads);
+      tc::mbar_init(&p_free[s], 1);
+      tc::mbar_init(&x_bar[s], kSoftmaxThreads);
+    }
     tc::mbar_init(&sum_bar, kSoftmaxThreads);
     tc::mbar_fence_init();
   }
   if (warp == kProducerWarp) tc::tmem_alloc(&tmem_slot, kTmemCols);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t tS[2] = {tmem + kColS0, tmem + kColS1};
+  const uint32_t tO = tmem + kColO, tQ = tmem + kColQ;
 
   // Softmax thread (row, hf): row = TMEM lane = 32 * (warp % 4) + lane; hf = column half.
   const bool smx = warp < kSoftmaxWarps;
@@ -115,21 +126,26 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   const bool row_ok = smx && qi < NG;
   const int node = row_ok ? qi / G : 0;
   const int qh = kvh * G + (row_ok ? qi % G : 0);
-  if (smx) {   // stage this row's half of Q (64 head dims), K-major with 128-byte swizzle
-    const uint16_t* qp = Q + (((size_t)b * N + node) * Hq + qh) * kD + hf * 64;
+  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+
+  if (smx) {
+    // Q row half (64 head dims) into TMEM as bf16 pairs: the S MMA reads A from TMEM.
+    const uint4* qp = reinterpret_cast<const uint4*>(Q + (((size_t)b * N + node) * Hq + qh) * kD + hf * 64);
+    uint32_t qv[32];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      uint4 v = row_ok ? *reinterpret_cast<const uint4*>(qp + c * 8) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(Qs + hf * kHalf + row * 128 + ((c ^ (row & 7)) << 4)) = v;
+      const uint4 v = row_ok ? qp[c] : make_uint4(0, 0, 0, 0);
+      qv[4 * c] = v.x;
+      qv[4 * c + 1] = v.y;
+      qv[4 * c + 2] = v.z;
+      qv[4 * c + 3] = v.w;
     }
-    tc::fence_proxy_async();
+    tc::tmem_st32(tQ + lane_base + hf * 32, qv);
+    tc::tmem_wait_st();
   }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  const uint32_t tmem = tmem_slot;
-  const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO = tmem + 256;
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
@@ -137,8 +153,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       const int head_row = (b * Hkv + kvh) * L_cap;
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !tc::mbar_wait(&kv_empty[s], ((j - 2) >> 1) & 1, err, 1)) break;
+        const int s = j % kStages;
+        if (j >= kStages && !tc::mbar_wait(&kv_empty[s], ((j / kStages) - 1) & 1, err, 1)) break;
         const int row0 = j < ptiles ? head_row + k_begin + j * kKeys : head_row + Lb;
         tc::mbar_arrive_expect(&kv_full[s], 2 * kTile);
         tc::tma_load_2d(Ks + s * kTile, &tmK, 0, row0, &kv_full[s]);
@@ -148,48 +164,47 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         issued = j + 1;
       }
       // Drain: never leave the CTA with tile loads still landing in shared memory.
-      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j) tc::mbar_wait(&kv_full[j & 1], (j >> 1) & 1, err, 128);
+      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+        tc::mbar_wait(&kv_full[j % kStages], (j / kStages) & 1, err, 128);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
       constexpr uint32_t idS = tc::idesc_bf16_f32(kRows, kKeys, 0, 0);
       constexpr uint32_t idPV = tc::idesc_bf16_f32(kRows, kD, 0, 1);
-      const uint32_t qa = tc::saddr(Qs), pa = tc::saddr(Ps);
       for (int j = 0; j <= ntiles; ++j) {
         if (j < ntiles) {
-          const int s = j & 1;
-          if (!tc::mbar_wait(&kv_full[s], (j >> 1) & 1, err, 2)) break;
-          if (j >= 2 && !tc::mbar_wait(&s_free[s], ((j - 2) >> 1) & 1, err, 4)) break;
+          const int ks = j % kStages, s = j & 1;
+          if (!tc::mbar_wait(&kv_full[ks], (j / kStages) & 1, err, 2)) break;
+          // S slot j&1 still holds P_{j-2} until PV_{j-2} has completed
+          if (j >= 2 && !tc::mbar_wait(&p_free[s], ((j - 2) >> 1) & 1, err, 4)) break;
           tc::fence_after();
-          const uint32_t ka = tc::saddr(Ks + s * kTile);
+          const uint32_t ka = tc::saddr(Ks + ks * kTile);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            tc::mma_bf16(tS[s], tc::sw128_desc(qa + off, 16, 1024), tc::sw128_desc(ka + off, 16, 1024), idS, kk > 0);
+            tc::mma_bf16_tmem_a(tS[s], tQ + kk * 8, tc::sw128_desc(ka + off, 16, 1024), idS, kk > 0);
           }
           tc::commit(&s_full[s]);
         }
         if (j >= 1) {
-          const int jp = j - 1, s = jp & 1;
-          if (!tc::mbar_wait(&p_full, jp & 1, err, 8)) break;
+          const int jp = j - 1, ks = jp % kStages, s = jp & 1;
+          if (!tc::mbar_wait(&p_full[s], (jp >> 1) & 1, err, 8)) break;
           tc::fence_after();
-          const uint32_t va = tc::saddr(Vs + s * kTile);
+          const uint32_t va = tc::saddr(Vs + ks * kTile);
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk) {
-            const uint64_t ad = tc::sw128_desc(pa + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
             const uint64_t bd = tc::sw128_desc(va + kk * 2048, kHalf, 1024);
-            tc::mma_bf16(tO, ad, bd, idPV, (jp > 0 || kk > 0) ? 1 : 0);
+            tc::mma_bf16_tmem_a(tO, tS[s] + kk * 8, bd, idPV, (jp > 0 || kk > 0) ? 1 : 0);
           }
-          tc::commit(&kv_empty[s]);
-          tc::commit(&o_done);
+          tc::commit(&kv_empty[ks]);
+          tc::commit(&p_free[s]);
         }
       }
     }
   } else {
     // ------------------------------------------------------------------ softmax warps
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t col0 = hf * 64;                // this thread's S / O / P columns
+    const uint32_t col0 = hf * 64;                // this thread's S / O columns
     const uint64_t nbits = hf ? bits[2 * node + 1] : bits[2 * node];   // tree keys of this column half
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -205,8 +220,6 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       tc::tmem_ld32(tS[s] + lane_base + col0, sv);
       tc::tmem_ld32(tS[s] + lane_base + col0 + 32, sv + 32);
       tc::tmem_wait_ld();
-      tc::fence_before();
-      tc::mbar_arrive(&s_free[s]);
 
       const bool tree = j >= ptiles;
       const int nkeys = tree ? N : min(kKeys, k_end - (k_begin + j * kKeys));
@@ -226,8 +239,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       for (int k = 8; k < 64; ++k) m8[k & 7] = fmaxf(m8[k & 7], __uint_as_float(sv[k]));
       float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       xmax[s][hf][row] = mx;
+      // Arriving here also tells the partner thread that this half of S_j has been read.
+      tc::fence_before();
       tc::mbar_arrive(&x_bar[s]);
       ok = tc::mbar_wait(&x_bar[s], (j >> 1) & 1, err, 256);
+      tc::fence_after();
       mx = fmaxf(mx, xmax[s][hf ^ 1][row]);
 
       const float m_tile = mx * scale_log2;
@@ -253,35 +269,31 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       }
       l_run = l_run * corr + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
 
-      if (j >= 1) {
-        ok = tc::mbar_wait(&o_done, (j - 1) & 1, err, 32);
+      if (j >= 1 && __any_sync(0xffffffffu, corr != 1.f)) {
+        // O is rescaled only after every earlier PV product has landed (PV_{j-1} is the last one).
+        ok = tc::mbar_wait(&p_free[(j - 1) & 1], ((j - 1) >> 1) & 1, err, 64);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
         tc::fence_after();
-        if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t ov[32];
-            tc::tmem_ld32(tO + lane_base + col0 + c * 32, ov);
-            tc::tmem_wait_ld();
+        for (int c = 0; c < 2; ++c) {
+          uint32_t ov[32];
+          tc::tmem_ld32(tO + lane_base + col0 + c * 32, ov);
+          tc::tmem_wait_ld();
 #pragma unroll
-            for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * corr);
-            tc::tmem_st32(tO + lane_base + col0 + c * 32, ov);
-          }
-          tc::tmem_wait_st();
+          for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * corr);
+          tc::tmem_st32(tO + lane_base + col0 + c * 32, ov);
         }
       }
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(Ps + hf * kHalf + row * 128 + ((c ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      tc::fence_proxy_async();
+      // P_j (this half: keys 64*hf .. +63) over the first 64 columns of the S slot.
+      tc::tmem_st32(tS[s] + lane_base + hf * 32, pk);
+      tc::tmem_wait_st();
       tc::fence_before();
-      tc::mbar_arrive(&p_full);
+      tc::mbar_arrive(&p_full[s]);
     }
-    if (ok && ntiles > 0) ok = tc::mbar_wait(&o_done, (ntiles - 1) & 1, err, 64);
+    if (ok && ntiles > 0) ok = tc::mbar_wait(&p_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, err, 64);
     const bool have = __all_sync(0xffffffffu, ok) && ntiles > 0;
     tc::fence_after();
     xsum[hf][row] = l_run;
