@@ -37,9 +37,10 @@ UNIT = "steps/s"
 DEFAULT_WORKLOAD = "vicuna7b_b1"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes per launch of the dominant call from the committed ncu capture, by
-# workload; None until a capture of the current kernels exists.
-NCU_TRAFFIC_BYTES = {}
+# DRAM bytes per medusa_heads call, from the committed ncu capture of the heads
+# kernels on a reduced vocabulary (V=8000: traffic 1.02x the algorithmic
+# weight bytes), scaled to the workload's weight rows. Absent = not captured.
+NCU_TRAFFIC_BYTES = {"vicuna7b_b1": int(1.02 * 1182801920)}
 
 
 def parse():
@@ -52,6 +53,12 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager launches instead of one CUDA graph")
+    ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed steps before the timed region")
+    ap.add_argument("--part", default="step", choices=["step", "heads", "attention", "verify"],
+                    help="diagnostic: time one library call in a loop (for profiler captures)")
+    ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
+                    help="diagnostic: override a workload field (e.g. V=8000, B=4)")
     return ap.parse_args()
 
 
@@ -226,6 +233,50 @@ def make_targets(w, si, dev, mode, seed, via_library=True):
     return synth.target_logits(w, seed, device=dev, zhat=zhat, depth=depth)
 
 
+def workload_of(args):
+    w = configs.get(args.workload)
+    if args.set:
+        kv = {}
+        for item in args.set:
+            k, v = item.split("=", 1)
+            kv[k] = type(getattr(w, k))(v) if not isinstance(getattr(w, k), tuple) else tuple(int(x) for x in v.split(","))
+        w = configs.scaled(w, **kv)
+    return w
+
+
+def run_part(args):
+    """Diagnostic: one library call of the workload, timed in a loop (eager launches)."""
+    from medusa_speculative_decoding_heads_gb300 import _build, binding as mb
+    from medusa_speculative_decoding_heads_gb300.step import DeviceStep, to_device_inputs
+    _build.build()
+    mb.load()
+    dev = torch.device("cuda")
+    w = workload_of(args)
+    mode = w.modes[0]
+    si = synth.make_step_inputs(w, seed=args.seed, device=dev)
+    st = DeviceStep(w, mode, si.L_cap, dev)
+    L = torch.from_numpy(si.L).to(dev)
+    st.heads(si.h, si.W, si.bias, si.U, write_logits=True)
+    st.tree_build(torch.from_numpy(si.root_token).to(dev), L)
+    tl = make_targets(w, si, dev, mode, args.seed) if args.part == "verify" else None
+    ua, ur = (torch.from_numpy(x).to(dev) for x in (si.u_acc, si.u_res))
+    call = {"heads": lambda: st.heads(si.h, si.W, si.bias, si.U, write_logits=mode == REJECTION),
+            "attention": lambda: st.tree_attention(si.Q, si.Kc, si.Vc, L),
+            "verify": lambda: st.verify(tl, ua, ur)}[args.part]
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    print(json.dumps({"part": args.part, "workload": w.name, "overrides": args.set, "us_per_call": 1000 * ms}))
+    return 0
+
+
 def run_ours(args):
     from medusa_speculative_decoding_heads_gb300 import _build, binding as mb
     from medusa_speculative_decoding_heads_gb300.step import DeviceStep, to_device_inputs
@@ -267,31 +318,59 @@ def run_ours(args):
         inp.L.copy_(L0, non_blocking=True)
         for i, call in enumerate(calls):
             if marks is not None:
-                marks[i].record(stream)
+                marks[i].record()          # on the current stream (the capture stream inside a graph)
             call()
         if marks is not None:
-            marks[len(calls)].record(stream)
+            marks[len(calls)].record()
 
     for _ in range(max(3, args.warmup)):
         one_step()
     torch.cuda.synchronize()
     acc = st.acc.cpu().numpy()
 
-    marks = [[ev() for _ in range(len(calls) + 1)] for _ in range(args.steps)]
-    t0, t1 = ev(), ev()
     sampler = ClockSampler(local) if rank == 0 else None
+    timed = None
+    if not args.eager:
+        try:
+            timed = time_graph(one_step, len(calls), args.steps, stream, mb)
+        except Exception as exc:  # graph capture unavailable: fall back to eager launches
+            print(f"# CUDA graph capture failed ({exc!r}); timing eager launches", file=sys.stderr)
+            timed = None
     if sampler:
         sampler.start()
+    # Soak: ~1 s of the same step right before the timed region, so the clock
+    # samples (every 200 ms) see the GPU under this load.
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak:
+        if timed is not None:
+            timed[0].replay()
+        else:
+            for _ in range(args.steps):
+                one_step()
+        torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    n0 = mb.launch_count()
-    t0.record(stream)
-    for k in range(args.steps):
-        one_step(marks[k])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    launches = mb.launch_count() - n0
+    if timed is not None:
+        graph, marks, launches_per_step = timed
+        t0, t1 = ev(), ev()
+        t0.record(stream)
+        graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        launches = launches_per_step * args.steps
+        launch_mode = "cuda_graph"
+    else:
+        marks = [[ev() for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+        t0, t1 = ev(), ev()
+        n0 = mb.launch_count()
+        t0.record(stream)
+        for k in range(args.steps):
+            one_step(marks[k])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        launches = mb.launch_count() - n0
+        launch_mode = "eager"
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
@@ -327,7 +406,7 @@ def run_ours(args):
                    "temperature": w.temperature if mode == REJECTION else None,
                    "l2": f"inputs larger than L2 ({by['total'] / 1e9:.2f} GB algorithmic per step)",
                    "parallelism": f"replicas x{world}"},
-        "clocks": clocks,
+        "clocks": dict(clocks or {}, window=f"{args.soak:.1f} s soak of the same step + the timed region"),
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "kernel": "medusa_heads (residual + vocab projection GEMV, top-s)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
@@ -336,6 +415,7 @@ def run_ours(args):
         "step_roofline": {"algorithmic_bytes": by["total"], "achieved_gbs": by["total"] / (ms_per_step * 1e-3) / 1e9,
                           "frac": by["total"] / (ms_per_step * 1e-3) / 1e9 / hbm, "bytes_by_term": by},
         "breakdown_ms": dict(per_call, step=ms_per_step),
+        "launch_mode": launch_mode,
         "accepted_per_step": float(np.mean(acc + 1)),
         "e2e": e2e,
     }
@@ -345,6 +425,22 @@ def run_ours(args):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def time_graph(one_step, ncalls, steps, stream, mb):
+    """Capture `steps` consecutive steps as one CUDA graph, with timing events
+    recorded as graph nodes around every library call of every step."""
+    mk = lambda: torch.cuda.Event(enable_timing=True, external=True)
+    marks = [[mk() for _ in range(ncalls + 1)] for _ in range(steps)]
+    graph = torch.cuda.CUDAGraph()
+    n0 = mb.launch_count()
+    with torch.cuda.graph(graph):
+        for k in range(steps):
+            one_step(marks[k])
+    launches_per_step = (mb.launch_count() - n0) // steps
+    graph.replay()                      # one untimed replay
+    torch.cuda.synchronize()
+    return graph, marks, launches_per_step
 
 
 def run_e2e(w, st, inp, L0, tl, si, args, stream, world):
@@ -381,14 +477,29 @@ def run_e2e(w, st, inp, L0, tl, si, args, stream, world):
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
-    steps = max(5, args.steps // 2)
+    steps = args.steps
+    graph = None
+    if not args.eager:
+        try:   # the same launches, copies included, captured once and replayed
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for _ in range(steps):
+                    e2e_step()
+            graph.replay()
+            torch.cuda.synchronize()
+        except Exception as exc:
+            print(f"# e2e graph capture failed ({exc!r}); timing eager launches", file=sys.stderr)
+            graph = None
     if world > 1:
         torch.distributed.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     a.record(stream)
-    for _ in range(steps):
-        e2e_step()
+    if graph is not None:
+        graph.replay()
+    else:
+        for _ in range(steps):
+            e2e_step()
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
@@ -397,7 +508,7 @@ def run_e2e(w, st, inp, L0, tl, si, args, stream, world):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
     return {"value": world * steps / (ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": steps}
+            "d2h_bytes_per_step": int(d2h), "steps": steps, "launch_mode": "cuda_graph" if graph else "eager"}
 
 
 def cpu_baseline(w, mode, si, tl):
@@ -411,6 +522,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.part != "step":
+        return run_part(args)
     return run_ours(args)
 
 
