@@ -47,7 +47,7 @@ AttnPlan plan_attention(const medusa_cfg& c) {
   const int path = attention_path(c);
   int tile = kKeyTile;
   if (path == kPathTc) {
-    p.row_groups = attention_tc_mtiles(p.NG);
+    p.row_groups = attention_tc_ctas_x(p.NG);
     tile = 128;
   } else if (path == kPathMma) {
     attention_mma_warps(p.NG, &p.row_groups);
@@ -56,8 +56,11 @@ AttnPlan plan_attention(const medusa_cfg& c) {
     p.row_groups = (p.NG + kRowsPerCta - 1) / kRowsPerCta;
   }
   const int Lmax = c.L_cap - ts.N;   // longest committed prefix that fits
+  // Split the KV range only while the whole grid still fits one wave (one CTA
+  // per SM): every CTA pays a pipeline fill and an epilogue, and splits add a
+  // merge pass, so beyond one wave more splits cost more than they balance.
   const long ctas = (long)p.row_groups * c.Hkv * c.B;
-  int want = (int)((2L * 152 + ctas - 1) / ctas);
+  int want = (int)(152 / ctas);
   int by_len = (Lmax + 255) / 256;
   p.nsplit = want < by_len ? want : by_len;
   if (p.nsplit > 32) p.nsplit = 32;   // the merge gives one lane per split
@@ -218,6 +221,7 @@ __global__ void tree_attn_merge_kernel(const float* __restrict__ o_part, const f
 #pragma unroll 4
   for (int s = 0; s < nsplit; ++s) {
     const float ws = __shfl_sync(0xffffffffu, w, s);
+    if (ws == 0.f) continue;   // an empty split need not have written its partial O
     const float* op = o_part + (row0 + s * split_stride) * D;
 #pragma unroll
     for (int j = 0; j < D / 32; ++j) acc[j] += op[lane + 32 * j] * ws;

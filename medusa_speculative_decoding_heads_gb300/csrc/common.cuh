@@ -96,6 +96,7 @@ cudaError_t launch_attention(const medusa_cfg& c, const void* Q, const void* Kc,
 size_t attention_workspace(const medusa_cfg& c);
 int attention_mma_warps(int NG, int* row_blocks);
 int attention_tc_mtiles(int NG);
+int attention_tc_ctas_x(int NG);
 cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, const void* Q, const void* Kc,
                                 const void* Vc, const int32_t* L, const uint64_t* bits, float* o_part, float* ml_part,
                                 void* O, cudaStream_t st);

@@ -33,13 +33,26 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 
+// One try_wait without a suspend hint: cheaper when the phase is usually
+// already complete (the issuing warps of a pipeline).
+__device__ __forceinline__ bool mbar_try_short(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+               : "=r"(ok)
+               : "r"(saddr(b)), "r"(parity)
+               : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete, for at most ~`budget`
 // clock cycles. Returns false (and ORs `code` into *err) when the budget runs out.
+template <bool kShort = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint32_t* err, uint32_t code,
                                           long long budget = 4000000000LL) {
-  if (mbar_try(b, parity)) return true;
+  auto probe = [&]() { return kShort ? mbar_try_short(b, parity) : mbar_try(b, parity); };
+  if (probe()) return true;
   const long long t0 = clock64();
-  while (!mbar_try(b, parity)) {
+  while (!probe()) {
     if (clock64() - t0 > budget) {
       if (err) atomicOr(err, code);
       return false;
@@ -96,6 +109,12 @@ __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
                : "memory");
+}
+// One lane of a converged warp (elect.sync): the lane that issues tcgen05.mma / commit.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile("{ .reg .pred e; elect.sync _|e, 0xffffffff; selp.u32 %0, 1, 0, e; }" : "=r"(p));
+  return p != 0;
 }
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
