@@ -6,8 +6,8 @@
  *   1. K Medusa heads on the backbone's last hidden state h: a residual block
  *      r_k = h + SiLU(W_k h + b_k) and a vocab projection z_k = U_k r_k, then a
  *      top-s_k list per head  ["Medusa 심층 아키텍처" (techknowgenie), section
- *      "Medusa의 핵심 철학", equations h_t^(k) and p_k; section "소스코드 레벨 구조
- *      분석", MedusaHead and generate_candidates].
+ *      "잔차 블록(Residual Block)을 포함한 Medusa 헤드 구조", equations h_t^(k) and
+ *      p_k; section "소스코드 레벨 구조 분석", MedusaHead and generate_candidates].
  *   2. The Cartesian candidate tree, its ancestor mask and position ids
  *      [same page, section "트리 어텐션", tree-topology example and the TreeMask
  *      equation].

@@ -1,9 +1,10 @@
 // Medusa heads: residual block, vocab projection and per-head top-s.
 //
-// "Medusa 심층 아키텍처" (techknowgenie), section "Medusa의 핵심 철학", equations
-// h_t^(k) = SiLU(h_t W_res^(k)) + h_t and p_k = softmax(h_t^(k) W_head^(k)); the
-// section "소스코드 레벨 구조 분석" (MedusaHead: Linear(d,d), SiLU, + residual,
-// Linear(d,V); generate_candidates: torch.topk(...).indices per head).
+// "Medusa 심층 아키텍처" (techknowgenie), section "잔차 블록(Residual Block)을
+// 포함한 Medusa 헤드 구조", equations h_t^(k) = SiLU(h_t W_res^(k)) + h_t and
+// p_k = softmax(h_t^(k) W_head^(k)); the section "소스코드 레벨 구조 분석"
+// (MedusaHead: Linear(d,d), SiLU, + residual, Linear(d,V); generate_candidates:
+// torch.topk(...).indices per head).
 //
 // Both projections are "many weight rows times a handful of vectors": the
 // weights stream from HBM exactly once and each weight row meets all B input

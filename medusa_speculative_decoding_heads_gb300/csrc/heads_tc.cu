@@ -1,6 +1,7 @@
 // Medusa heads on tcgen05 tensor cores with TMA-fed weight streaming.
 //
-// "Medusa 심층 아키텍처" (techknowgenie), section "Medusa의 핵심 철학", equations
+// "Medusa 심층 아키텍처" (techknowgenie), section "잔차 블록(Residual Block)을 포함한
+// Medusa 헤드 구조", equations
 // h_t^(k) = SiLU(h_t W_res^(k)) + h_t and p_k = softmax(h_t^(k) W_head^(k)).
 //
 // Both projections are weight-streaming GEMVs: every weight byte is read once

@@ -70,7 +70,8 @@ def silu(x: np.ndarray) -> np.ndarray:
 def medusa_heads(h: np.ndarray, W: np.ndarray, b: Optional[np.ndarray], U: np.ndarray):
     """Residual block then vocab projection for every head.
 
-    [MEDUSA-ARCH] "Medusa의 핵심 철학" section, equations for h_t^(k) and p_k:
+    [MEDUSA-ARCH] "잔차 블록(Residual Block)을 포함한 Medusa 헤드 구조" section,
+    equations for h_t^(k) and p_k:
     h^(k) = SiLU(h W_res^(k)) + h and p_k = softmax(h^(k) W_head^(k)); the
     "소스코드 레벨 구조 분석" section's MedusaHead applies Linear(d, d), SiLU,
     adds the residual, then Linear(d, V) without bias. A per-head bias b_k on
