@@ -72,6 +72,8 @@ enum {
 #define MEDUSA_FLAG_RS_NEAR_TIE 1u  /* some acceptance test had |u - r| < 1e-6            */
 #define MEDUSA_FLAG_CDF_NEAR_TIE 2u /* an inverse-CDF draw fell within 1e-6*total of a step */
 #define MEDUSA_FLAG_CAPACITY 4u     /* L_b < 0 or L_b + N > L_cap: sequence skipped      */
+#define MEDUSA_FLAG_TIMEOUT 8u      /* a bounded device-side wait gave up: outputs of this */
+                                    /* sequence are not valid                              */
 
 typedef struct {
   int32_t B;            /* sequences in the step                                 */
@@ -151,10 +153,14 @@ MEDUSA_API int medusa_tree_attention(const medusa_cfg* cfg, const void* Q, const
  * Outputs: acc [B] accepted drafts; path [B][K+1] node ids (path[0] = 0, -1 pad);
  *   out_tokens [B][K+1] the accepted tokens then the bonus/correction token
  *   (-1 pad); n_out [B] = acc + 1; flags [B] uint32: this call ORs in its
- *   MEDUSA_FLAG_* bits (clear or initialise it first, e.g. with medusa_tree_build).
- * Every tree node's target row is reduced in parallel first (argmax, or row max
- * and softmax normaliser), so the serial walk only sweeps rows on rejection
- * and for the final draw.
+ *   MEDUSA_FLAG_* bits (clear or initialise it first, e.g. with medusa_tree_build);
+ *   MEDUSA_FLAG_TIMEOUT marks a sequence whose walk gave up on a bounded wait.
+ * GREEDY reduces every tree node's target row to its argmax in parallel first,
+ * so the walk itself is a few table lookups. REJECTION reduces every head row
+ * (max and softmax normaliser) in parallel first; each sequence's walk then runs
+ * on a cluster of up to 8 CTAs that split the vocabulary, trading their partial
+ * sums through distributed shared memory: one sweep of the visited target row
+ * per depth, one more per rejection and one for the final draw.
  * GREEDY: the child whose token equals argmax(target_logits[node]) (ties to
  * the lowest id) is accepted until none matches; the bonus is that argmax at
  * the last accepted node.

@@ -16,10 +16,11 @@
 // Two launches per call. Greedy: every tree node's target-row argmax in
 // parallel (one CTA per row), then a one-thread-per-sequence walk. Rejection
 // sampling: the max and softmax normaliser of every head's logit row in
-// parallel, then one CTA per sequence walks; at each visited node one sweep
-// gives the target row's max and normaliser, an acceptance test is O(1), and
-// only a rejection (the residual's normaliser) and the final draw (inverse CDF)
-// sweep the row again. Bulk sums use the hardware base-2 exponential; the
+// parallel, then one cluster of CTAs per sequence walks, each CTA owning a slice
+// of the vocabulary; at each visited node one sweep gives the target row's max
+// and normaliser, an acceptance test is O(1), and only a rejection (the
+// residual's normaliser) and the final draw (inverse CDF) sweep the row again.
+// The slices' partial results meet through distributed shared memory. Bulk sums use the hardware base-2 exponential; the
 // acceptance ratios use the accurate one.
 // Sums use compensated float32 pairs: float64 is slow on this part and plain
 // float32 prefix sums over 32k entries drift by ~1e-6 of the total, the width
@@ -358,12 +359,79 @@ __global__ void greedy_walk_kernel(TreeShape ts, int B, const int32_t* __restric
   w.n_out[b] = acc + 1;
 }
 
-constexpr int kVThreads = 1024;
+constexpr int kVThreads = 256;
 constexpr int kVWarps = kVThreads / 32;
 // Padded row stride of the inverse-CDF transpose: entry v sits at
 // buf[(v % C) * kPad + v / C] so that both the scattered writes and the
 // contiguous per-thread reads are free of bank conflicts.
 constexpr int kPad = kVThreads + 1;
+constexpr int kMaxCluster = 8;   // CTAs per sequence (portable cluster size)
+
+// ---------------------------------------------------------------- cluster exchange
+// The CTAs of one cluster share one sequence's walk: CTA r owns the vocabulary
+// slice [r * S, (r + 1) * S). Block-level partials are traded through
+// distributed shared memory: thread r stores this CTA's value into slot[rank]
+// of CTA r and arrives (release, cluster scope) on CTA r's mbarrier; every CTA
+// waits (acquire, bounded) for all arrivals and reads the slots in rank order,
+// so all CTAs combine the same numbers in the same order and take identical
+// decisions. Two barriers alternate, so a CTA can run at most one exchange ahead.
+struct Xchg {
+  uint64_t bar[2];
+  float2 f[2][kMaxCluster];
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ void tc_free_mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ uint32_t cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_ctas() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t remote(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// All threads call with the same block-uniform value; returns every CTA's value in vals[rank].
+__device__ void xchg(Xchg& x, int& xn, float2 mine, float2* vals, uint32_t ncta, uint32_t rank, uint32_t* fl) {
+  const int par = xn & 1;
+  __syncthreads();
+  if (threadIdx.x < ncta) {
+    const uint32_t slot = remote(&x.f[par][rank], threadIdx.x);
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(slot), "f"(mine.x), "f"(mine.y) : "memory");
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote(&x.bar[par], threadIdx.x))
+                 : "memory");
+  }
+  const uint32_t parity = (xn >> 1) & 1;
+  const uint32_t baddr = smem_u32(&x.bar[par]);
+  uint32_t ok = 0;
+  const long long t0 = clock64();
+  while (true) {
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(baddr), "r"(parity)
+        : "memory");
+    if (ok) break;
+    if (clock64() - t0 > 4000000000LL) {   // a peer never arrived: record it and carry on
+      *fl |= MEDUSA_FLAG_TIMEOUT;
+      break;
+    }
+  }
+  for (uint32_t r = 0; r < ncta; ++r) vals[r] = x.f[par][r];
+  ++xn;
+}
 
 // State of the walk at one depth: p_0 = softmax(target[cur] / T), q = softmax(head / T),
 // and p_j = max(0, p_{j-1} - q) / Z_j after j rejections (p_j = p_{j-1} when Z_j < 1e-30).
@@ -378,15 +446,6 @@ __device__ __forceinline__ float apply_levels(const WalkState& ws, float p, floa
   for (int j = 1; j <= ws.levels; ++j)
     if (ws.kept[j]) p = fmaxf(0.f, p - q) * ws.inv_zr[j];
   return p;
-}
-
-// One entry with the accurate exponential (acceptance tests).
-template <typename T>
-__device__ __forceinline__ float p_exact(const WalkState& ws, const T* trow, const float* hrow, float Tmp, int v,
-                                         float* qv) {
-  const float q = hrow ? expf((hrow[v] - ws.mq) / Tmp) * ws.inv_zq : 0.f;
-  *qv = q;
-  return apply_levels(ws, expf((Elt<T>::load(trow, v) - ws.mt) / Tmp) * ws.inv_zt, q);
 }
 
 // One entry / 8 consecutive entries with the fast exponential (row sweeps); c = log2(e) / T.
@@ -411,86 +470,181 @@ __device__ __forceinline__ void p_fast8(const WalkState& ws, const T* trow, cons
   }
 }
 
-// Row max and softmax normaliser of a target row in one sweep: per-thread
-// (max, sum exp) pairs merged across the block by rescaling to the larger max.
-template <typename T, int C, bool VEC>
-__device__ float2 target_stats(const T* trow, int V, float c, Scratch<kVWarps>& s, float* pm, float* ps) {
-  float mx = -INFINITY;
-  FF sum{0.f, 0.f};
-  if (VEC) {
-#pragma unroll 1
-    for (int i = 0; i < C / 8; ++i) {
-      const int v0 = 8 * (threadIdx.x + i * kVThreads);
-      if (v0 >= V) break;
-      float x[8];
-      load8<T>(trow, v0, x);
-      float m8 = x[0];
+// Entry v of this CTA's slice for thread t, step i: VEC takes 8 consecutive
+// entries per step (v0 = lo + 8 (t + i * kVThreads)), otherwise one (lo + t + i * kVThreads).
+
+// (max, sum of 2^((v - max) c)) pairs merged by rescaling to the larger max.
+struct MS {
+  float m;
+  FF s;
+};
+__device__ __forceinline__ MS ms_merge(MS a, MS b, float c) {
+  const float M = fmaxf(a.m, b.m);
+  if (M == -INFINITY) return a;
+  const float ra = a.m == -INFINITY ? 0.f : fast_exp2((a.m - M) * c);
+  const float rb = b.m == -INFINITY ? 0.f : fast_exp2((b.m - M) * c);
+  return MS{M, ff_add(FF{a.s.hi * ra, a.s.lo * ra}, FF{b.s.hi * rb, b.s.lo * rb})};
+}
+// One block-wide merge (a single round of shared memory) of every thread's pair.
+template <int NW>
+__device__ MS block_ms(MS v, float c, Scratch<NW>& s) {
 #pragma unroll
-      for (int e = 1; e < 8; ++e) m8 = fmaxf(m8, x[e]);
-      if (m8 > mx) {   // rescale the running sum to the new maximum
-        const float r = mx == -INFINITY ? 0.f : fast_exp2((mx - m8) * c);
-        sum = FF{sum.hi * r, sum.lo * r};
-        mx = m8;
-      }
+  for (int o = 16; o > 0; o >>= 1) {
+    const MS w{__shfl_xor_sync(0xffffffffu, v.m, o), ff_shfl_xor(v.s, o)};
+    v = ms_merge(v, w, c);
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    s.f[threadIdx.x >> 5] = v.m;
+    s.hi[threadIdx.x >> 5] = v.s.hi;
+    s.lo[threadIdx.x >> 5] = v.s.lo;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    MS w = threadIdx.x < NW ? MS{s.f[threadIdx.x], FF{s.hi[threadIdx.x], s.lo[threadIdx.x]}}
+                            : MS{-INFINITY, FF{0.f, 0.f}};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = fast_exp2((x[e] - mx) * c);
-      sum = ff_add8(sum, x);
+    for (int o = 16; o > 0; o >>= 1) {
+      const MS u{__shfl_xor_sync(0xffffffffu, w.m, o), ff_shfl_xor(w.s, o)};
+      w = ms_merge(w, u, c);
     }
-  } else {
-#pragma unroll 1
-    for (int i = 0; i < C; ++i) {
-      const int v = threadIdx.x + i * kVThreads;
-      if (v >= V) break;
-      const float x = Elt<T>::load(trow, v);
-      if (x > mx) {
-        const float r = mx == -INFINITY ? 0.f : fast_exp2((mx - x) * c);
-        sum = FF{sum.hi * r, sum.lo * r};
-        mx = x;
-      }
-      sum = ff_add(sum, fast_exp2((x - mx) * c));
+    if (threadIdx.x == 0) {
+      s.bf = w.m;
+      s.tot = w.s;
     }
   }
-  const float m = block_max(mx, s);
-  const float r = mx == -INFINITY ? 0.f : fast_exp2((mx - m) * c);
-  const FF z = block_sum_ff(FF{sum.hi * r, sum.lo * r}, s);
-  (void)pm;
-  (void)ps;
-  return make_float2(m, z.hi + z.lo);
+  __syncthreads();
+  return MS{s.bf, s.tot};
 }
 
-// Inverse CDF of the current p over the row; sets *near for the 1e-6 tie band.
+// Row max and softmax normaliser of a target row over this CTA's slice (all of
+// a thread's entries are loaded first, so their latencies overlap), merged across
+// the block and then across the cluster by rescaling to the larger max.
 template <typename T, int C, bool VEC>
-__device__ __forceinline__ int walk_inverse_cdf(const WalkState& ws, const T* trow, const float* hrow, float c,
-                                                int V, float u, float* buf, Scratch<kVWarps>& s, bool* near) {
-  __syncthreads();
-  if (VEC) {   // entries v = 8 * (t + i * kVThreads) + e
-#pragma unroll 1
+__device__ float2 target_stats(const T* trow, int lo, int hi, float c, Scratch<kVWarps>& s, Xchg& x, int& xn,
+                               uint32_t ncta, uint32_t rank, uint32_t* fl) {
+  float xv[C];
+  if (VEC) {
+#pragma unroll
     for (int i = 0; i < C / 8; ++i) {
-      const int v0 = 8 * (threadIdx.x + i * kVThreads);
+      const int v0 = lo + 8 * (threadIdx.x + i * kVThreads);
+      if (v0 < hi) load8<T>(trow, v0, xv + 8 * i);
+      else
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xv[8 * i + e] = -INFINITY;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      const int v = lo + threadIdx.x + i * kVThreads;
+      xv[i] = v < hi ? Elt<T>::load(trow, v) : -INFINITY;
+    }
+  }
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < C; ++i) mx = fmaxf(mx, xv[i]);
+  FF sum{0.f, 0.f};
+  if (mx != -INFINITY) {
+#pragma unroll
+    for (int i = 0; i < C; i += 8) {
+      float e8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) e8[e] = (i + e < C) ? fast_exp2((xv[i + e] - mx) * c) : 0.f;
+      sum = ff_add8(sum, e8);
+    }
+  }
+  const MS blk = block_ms(MS{mx, sum}, c, s);
+  float2 vals[kMaxCluster];
+  xchg(x, xn, make_float2(blk.m, blk.s.hi + blk.s.lo), vals, ncta, rank, fl);
+  float M = -INFINITY;
+  for (uint32_t k = 0; k < ncta; ++k) M = fmaxf(M, vals[k].x);
+  FF Z{0.f, 0.f};
+  for (uint32_t k = 0; k < ncta; ++k)
+    if (vals[k].x != -INFINITY) Z = ff_add(Z, vals[k].y * fast_exp2((vals[k].x - M) * c));
+  return make_float2(M, Z.hi + Z.lo);
+}
+
+// Sum over the row of max(0, p_j - q) (the next residual's normaliser).
+template <typename T, int C, bool VEC>
+__device__ float residual_sum(const WalkState& ws, const T* trow, const float* hrow, float c, int lo, int hi,
+                              Scratch<kVWarps>& s, Xchg& x, int& xn, uint32_t ncta, uint32_t rank, uint32_t* fl) {
+  FF loc{0.f, 0.f};
+  if (VEC) {
+#pragma unroll
+    for (int i = 0; i < C / 8; ++i) {
+      const int v0 = lo + 8 * (threadIdx.x + i * kVThreads);
+      if (v0 < hi) {
+        float p[8], q[8];
+        p_fast8<T>(ws, trow, hrow, c, v0, p, q);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) p[e] = fmaxf(0.f, p[e] - q[e]);
+        loc = ff_add8(loc, p);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      const int v = lo + threadIdx.x + i * kVThreads;
+      if (v < hi) {
+        float q;
+        const float p = p_fast<T>(ws, trow, hrow, c, v, &q);
+        loc = ff_add(loc, fmaxf(0.f, p - q));
+      }
+    }
+  }
+  const FF tot = block_sum_ff(loc, s);
+  float2 vals[kMaxCluster];
+  xchg(x, xn, make_float2(tot.hi, tot.lo), vals, ncta, rank, fl);
+  FF all{0.f, 0.f};
+  for (uint32_t k = 0; k < ncta; ++k) all = ff_add(all, FF{vals[k].x, vals[k].y});
+  return all.hi + all.lo;
+}
+
+// Inverse CDF of the current p over the row (smallest y with cdf(y) > u * total);
+// sets *near for the 1e-6 tie band.
+template <typename T, int C, bool VEC>
+__device__ int walk_inverse_cdf(const WalkState& ws, const T* trow, const float* hrow, float c, int lo, int hi,
+                                int V, float u, float* buf, Scratch<kVWarps>& s, Xchg& x, int& xn, uint32_t ncta,
+                                uint32_t rank, uint32_t* fl, bool* near) {
+  __syncthreads();
+  // this CTA's slice, local index lv = v - lo, into the transpose
+  if (VEC) {
+#pragma unroll
+    for (int i = 0; i < C / 8; ++i) {
+      const int l0 = 8 * (threadIdx.x + i * kVThreads);
       float p[8], q[8];
-      if (v0 < V) p_fast8<T>(ws, trow, hrow, c, v0, p, q);
+      if (lo + l0 < hi) p_fast8<T>(ws, trow, hrow, c, lo + l0, p, q);
       else
 #pragma unroll
         for (int e = 0; e < 8; ++e) p[e] = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) buf[((v0 + e) % C) * kPad + (v0 + e) / C] = p[e];
+      for (int e = 0; e < 8; ++e) buf[((l0 + e) % C) * kPad + (l0 + e) / C] = p[e];
     }
   } else {
-#pragma unroll 1
+#pragma unroll
     for (int i = 0; i < C; ++i) {
-      const int v = threadIdx.x + i * kVThreads;
+      const int l = threadIdx.x + i * kVThreads;
       float q;
-      const float p = v < V ? p_fast<T>(ws, trow, hrow, c, v, &q) : 0.f;
-      buf[(v % C) * kPad + v / C] = p;
+      const float p = lo + l < hi ? p_fast<T>(ws, trow, hrow, c, lo + l, &q) : 0.f;
+      buf[(l % C) * kPad + l / C] = p;
     }
   }
   __syncthreads();
-  const int v0 = threadIdx.x * C;   // this thread now holds entries [v0, v0 + C)
+  const int l0 = threadIdx.x * C;   // this thread now holds local entries [l0, l0 + C)
   FF loc{0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < C; ++i) loc = ff_add(loc, buf[i * kPad + threadIdx.x]);
-  FF total;
-  FF cum = block_exscan_ff(loc, s, &total);
+  FF cta_total;
+  FF cum = block_exscan_ff(loc, s, &cta_total);
+  // offsets of the slices before this one, and the row total
+  float2 vals[kMaxCluster];
+  xchg(x, xn, make_float2(cta_total.hi, cta_total.lo), vals, ncta, rank, fl);
+  FF total{0.f, 0.f}, before{0.f, 0.f};
+  for (uint32_t k = 0; k < ncta; ++k) {
+    if (k == rank) before = total;
+    total = ff_add(total, FF{vals[k].x, vals[k].y});
+  }
+  cum = ff_add(before, cum);
   const float th = u * total.hi;
   const FF thr = ff_norm(th, fmaf(u, total.hi, -th) + u * total.lo);   // u * total as an exact pair
   const float band = 1e-6f * (total.hi + total.lo);
@@ -500,19 +654,29 @@ __device__ __forceinline__ int walk_inverse_cdf(const WalkState& ws, const T* tr
   for (int i = 0; i < C; ++i) {
     const FF cp = cum;
     cum = ff_add(cum, buf[i * kPad + threadIdx.x]);
-    if (cand == 0x7fffffff && v0 + i < V && ff_diff(cum, thr) > 0.f) {
-      cand = v0 + i;
+    if (cand == 0x7fffffff && lo + l0 + i < hi && ff_diff(cum, thr) > 0.f) {
+      cand = lo + l0 + i;
       d_at = ff_diff(cum, thr);
       d_prev = ff_diff(thr, cp);
     }
   }
-  const int y = block_min_i(cand, s);
+  const int y_cta = block_min_i(cand, s);
   __shared__ int near_flag;
   if (threadIdx.x == 0) near_flag = 0;
   __syncthreads();
-  if (cand == y && y != 0x7fffffff) near_flag = (d_at < band || (y > 0 && d_prev < band)) ? 1 : 0;
+  if (cand == y_cta && y_cta != 0x7fffffff) near_flag = (d_at < band || (y_cta > 0 && d_prev < band)) ? 1 : 0;
   __syncthreads();
-  *near = near_flag != 0;
+  // the first slice holding a crossing wins
+  xchg(x, xn, make_float2(__int_as_float(y_cta), __int_as_float(near_flag)), vals, ncta, rank, fl);
+  int y = 0x7fffffff, nf = 0;
+  for (uint32_t k = 0; k < ncta; ++k) {
+    const int yk = __float_as_int(vals[k].x);
+    if (yk < y) {
+      y = yk;
+      nf = __float_as_int(vals[k].y);
+    }
+  }
+  *near = nf != 0;
   if (y == 0x7fffffff) {   // only reachable if rounding left u*total at or above the last cumulative sum
     *near = true;
     return V - 1;
@@ -520,27 +684,87 @@ __device__ __forceinline__ int walk_inverse_cdf(const WalkState& ws, const T* tr
   return y;
 }
 
-// One CTA per sequence.
+// One cluster of CTAs per sequence; CTA `rank` owns the vocabulary slice
+// [rank * S, rank * S + S) with S = slice (a multiple of 8).
 template <typename T, int C, bool VEC>
 __global__ void __launch_bounds__(kVThreads, 1)
-rs_walk_kernel(TreeShape ts, int V, float Tmp, const int32_t* __restrict__ tokens,
+rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restrict__ tokens,
                const int32_t* __restrict__ first_child, const T* __restrict__ tl, const float* __restrict__ hl,
                const float2* __restrict__ hstats, const float* __restrict__ u_acc, const float* __restrict__ u_res,
                WalkOut w) {
   extern __shared__ float buf[];   // inverse-CDF transpose, [C][kPad]
   __shared__ Scratch<kVWarps> s;
   __shared__ WalkState ws;
+  __shared__ Xchg x;
   __shared__ int path[kMaxK + 1], out[kMaxK + 1];
-  const int b = blockIdx.x, N = ts.N, K = ts.K;
+  const uint32_t ncta = cluster_ctas(), rank = cta_rank();
+  const int b = blockIdx.x / ncta, N = ts.N, K = ts.K;
+  const int lo = min(V, (int)rank * slice), hi = min(V, lo + slice);
   const float c = 1.4426950408889634f / Tmp;
-  const int32_t* tok = tokens + (size_t)b * N;
+  // this sequence's tree tokens and the tree's first-child table, staged once
+  __shared__ int s_tok[kMaxN], s_fc[kMaxN];
+  for (int i = threadIdx.x; i < N; i += kVThreads) {
+    s_tok[i] = tokens[(size_t)b * N + i];
+    s_fc[i] = first_child[i];
+  }
   uint32_t fl = 0;
+  int xn = 0;
+  if (threadIdx.x == 0) {
+    tc_free_mbar_init(&x.bar[0], ncta);
+    tc_free_mbar_init(&x.bar[1], ncta);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    path[0] = 0;
+  }
+  cluster_sync();   // every CTA's barriers exist before any peer arrives on them
+  // the candidates of the current depth: token, its target and head logits, and
+  // the acceptance uniform, fetched before the row sweep so that their load
+  // latency overlaps it
+  __shared__ float cand_t[kMaxS], cand_h[kMaxS], cand_u[kMaxS];
+  __shared__ int cand_n;
+  __shared__ float2 cand_q;
   int cur = 0, acc = 0;
-  bool done = false;
-  if (threadIdx.x == 0) path[0] = 0;
-  for (int dep = 1; dep <= K + 1 && !done; ++dep) {
+  for (int dep = 1; dep <= K + 1; ++dep) {
     const T* trow = tl + ((size_t)b * N + cur) * V;
-    const float2 tst = target_stats<T, C, VEC>(trow, V, c, s, nullptr, nullptr);
+    __syncthreads();   // the previous depth's candidates have been read (and the staging is done)
+    // candidate j's logits and uniform: loads issued now, stored after the row sweep
+    const bool fetch = dep <= K && threadIdx.x < ts.s[dep];
+    float ct = 0.f, ch = 0.f, cu = 0.f;
+    float2 cq = make_float2(0.f, 0.f);
+    if (fetch) {
+      const int fc = s_fc[cur];
+      const int j = threadIdx.x;
+      const int xt = (fc >= 0 && fc + j < N) ? min(max(s_tok[fc + j], 0), V - 1) : 0;
+      ct = Elt<T>::load(trow, xt);
+      ch = hl[((size_t)b * K + (dep - 1)) * V + xt];
+      cu = u_acc[((size_t)b * K + (dep - 1)) * ts.s_max + j];
+      if (j == 0) cq = hstats[(size_t)b * K + dep - 1];
+    }
+    if (dep <= K) {
+      // warm L2 with this CTA's slice of every child's target row (the next depth reads one of them)
+      const int fc = s_fc[cur];
+      const int lines = ((hi - lo) * (int)sizeof(T) + 127) / 128;   // every prefetched line starts inside the slice
+      for (int t = threadIdx.x; t < ts.s[dep] * lines; t += kVThreads) {
+        const int j = t / lines, l = t % lines;
+        if (fc >= 0 && fc + j < N) {
+          const char* pr = reinterpret_cast<const char*>(tl + ((size_t)b * N + fc + j) * V + lo) + 128 * l;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(pr));
+        }
+      }
+    }
+    const float2 tst = target_stats<T, C, VEC>(trow, lo, hi, c, s, x, xn, ncta, rank, &fl);
+    if (fetch) {
+      const int fc = s_fc[cur];
+      const int j = threadIdx.x;
+      cand_t[j] = ct;
+      cand_h[j] = ch;
+      cand_u[j] = cu;
+      if (j == 0) {
+        int nc = 0;
+        while (nc < ts.s[dep] && fc >= 0 && fc + nc < N) ++nc;
+        cand_n = nc;
+        cand_q = cq;
+      }
+    }
     if (dep == K + 1) {
       // accepted leaf: the bonus is drawn from softmax(target[leaf] / T)
       __syncthreads();
@@ -551,8 +775,8 @@ rs_walk_kernel(TreeShape ts, int V, float Tmp, const int32_t* __restrict__ token
       }
       __syncthreads();
       bool near = false;
-      const int y = walk_inverse_cdf<T, C, VEC>(ws, trow, nullptr, c, V, u_res[(size_t)b * (K + 1) + K], buf, s,
-                                                &near);
+      const int y = walk_inverse_cdf<T, C, VEC>(ws, trow, nullptr, c, lo, hi, V, u_res[(size_t)b * (K + 1) + K], buf,
+                                                s, x, xn, ncta, rank, &fl, &near);
       if (near) fl |= MEDUSA_FLAG_CDF_NEAR_TIE;
       if (threadIdx.x == 0) out[acc] = y;
       break;
@@ -560,7 +784,7 @@ rs_walk_kernel(TreeShape ts, int V, float Tmp, const int32_t* __restrict__ token
     const float* hrow = hl + ((size_t)b * K + (dep - 1)) * V;
     __syncthreads();
     if (threadIdx.x == 0) {
-      const float2 q = hstats[(size_t)b * K + dep - 1];
+      const float2 q = cand_q;
       ws.mt = tst.x;
       ws.inv_zt = 1.f / tst.y;
       ws.mq = q.x;
@@ -568,45 +792,23 @@ rs_walk_kernel(TreeShape ts, int V, float Tmp, const int32_t* __restrict__ token
       ws.levels = 0;
     }
     __syncthreads();
-    const int fc = first_child[cur];
+    const int fc = s_fc[cur];
+    const int nc = cand_n;
     int accepted = -1;
-    for (int j = 0; j < ts.s[dep] && fc >= 0 && fc + j < N; ++j) {
+    for (int j = 0; j < nc; ++j) {
       const int child = fc + j;
-      const int x = min(max(tok[child], 0), V - 1);
-      float qx;
-      const float px = p_exact<T>(ws, trow, hrow, Tmp, x, &qx);
+      const float qx = expf((cand_h[j] - ws.mq) / Tmp) * ws.inv_zq;
+      const float px = apply_levels(ws, expf((cand_t[j] - ws.mt) / Tmp) * ws.inv_zt, qx);
       const float r = fminf(1.f, px / qx);
-      const float u = u_acc[((size_t)b * K + (dep - 1)) * ts.s_max + j];
+      const float u = cand_u[j];
       if (fabsf(u - r) < 1e-6f) fl |= MEDUSA_FLAG_RS_NEAR_TIE;
       if (u < r) {
         accepted = child;
         break;
       }
       // residual: Z_{j+1} = sum_v max(0, p_j(v) - q(v)) over the row
-      FF loc{0.f, 0.f};
-      if (VEC) {
-#pragma unroll 1
-        for (int i = 0; i < C / 8; ++i) {
-          const int v0 = 8 * (threadIdx.x + i * kVThreads);
-          if (v0 >= V) break;
-          float p[8], q[8];
-          p_fast8<T>(ws, trow, hrow, c, v0, p, q);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) p[e] = fmaxf(0.f, p[e] - q[e]);
-          loc = ff_add8(loc, p);
-        }
-      } else {
-#pragma unroll 1
-        for (int i = 0; i < C; ++i) {
-          const int v = threadIdx.x + i * kVThreads;
-          if (v >= V) break;
-          float q;
-          const float p = p_fast<T>(ws, trow, hrow, c, v, &q);
-          loc = ff_add(loc, fmaxf(0.f, p - q));
-        }
-      }
-      const FF tot = block_sum_ff(loc, s);
-      const float ft = tot.hi + tot.lo;
+      const float ft = residual_sum<T, C, VEC>(ws, trow, hrow, c, lo, hi, s, x, xn, ncta, rank, &fl);
+      __syncthreads();
       if (threadIdx.x == 0) {
         const int l = ws.levels + 1;
         ws.kept[l] = ft >= 1e-30f;
@@ -617,54 +819,81 @@ rs_walk_kernel(TreeShape ts, int V, float Tmp, const int32_t* __restrict__ token
     }
     if (accepted < 0) {
       bool near = false;
-      const int y = walk_inverse_cdf<T, C, VEC>(ws, trow, hrow, c, V, u_res[(size_t)b * (K + 1) + (dep - 1)], buf, s,
-                                                &near);
+      const int y = walk_inverse_cdf<T, C, VEC>(ws, trow, hrow, c, lo, hi, V, u_res[(size_t)b * (K + 1) + (dep - 1)],
+                                                buf, s, x, xn, ncta, rank, &fl, &near);
       if (near) fl |= MEDUSA_FLAG_CDF_NEAR_TIE;
       if (threadIdx.x == 0) out[acc] = y;
-      done = true;
       break;
     }
     cur = accepted;
     if (threadIdx.x == 0) {
-      out[acc] = tok[cur];
+      out[acc] = s_tok[cur];
       path[acc + 1] = cur;
     }
     ++acc;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (rank == 0 && threadIdx.x == 0) {
     w.acc[b] = acc;
     w.n_out[b] = acc + 1;
     for (int r = 0; r <= K; ++r) {
       w.path[(size_t)b * (K + 1) + r] = r <= acc ? path[r] : -1;
       w.out_tokens[(size_t)b * (K + 1) + r] = r <= acc ? out[r] : -1;
     }
-    w.flags[b] |= fl;
   }
+  // flags from every CTA (near ties are seen by the slice that owns them)
+  __shared__ uint32_t fl_all;
+  if (threadIdx.x == 0) fl_all = 0;
+  __syncthreads();
+  if (fl) atomicOr(&fl_all, fl);
+  __syncthreads();
+  if (threadIdx.x == 0 && fl_all) atomicOr(&w.flags[b], fl_all);
+  cluster_sync();   // no CTA leaves while a peer may still write into its shared memory
 }
 
 template <typename T, int C, bool VEC>
-cudaError_t launch_rs_walk_v(const medusa_cfg& c, const TreeShape& ts, const int32_t* tokens,
+cudaError_t launch_rs_walk_v(const medusa_cfg& c, const TreeShape& ts, int ncta, int slice, const int32_t* tokens,
                              const int32_t* first_child, const void* tl, const float* hl, const float2* stats,
                              const float* ua, const float* ur, const WalkOut& w, cudaStream_t st) {
   const size_t smem = (size_t)C * kPad * sizeof(float);
-  cudaError_t e =
-      cudaFuncSetAttribute(rs_walk_kernel<T, C, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = rs_walk_kernel<T, C, VEC>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  rs_walk_kernel<T, C, VEC><<<c.B, kVThreads, smem, st>>>(ts, c.V, c.temperature, tokens, first_child,
-                                                          static_cast<const T*>(tl), hl, stats, ua, ur, w);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c.B * ncta);
+  cfg.blockDim = dim3(kVThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ncta;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, ts, c.V, slice, c.temperature, tokens, first_child, static_cast<const T*>(tl), hl,
+                         stats, ua, ur, w);
   note_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-// Vector loads need V % 8 == 0 (aligned rows) and at least 8 entries per thread.
+// Vector loads need V % 8 == 0 (aligned rows and slices) and at least 8 entries per thread.
 template <typename T, int C>
-cudaError_t launch_rs_walk(const medusa_cfg& c, const TreeShape& ts, const int32_t* tokens, const int32_t* first_child,
-                           const void* tl, const float* hl, const float2* stats, const float* ua, const float* ur,
-                           const WalkOut& w, cudaStream_t st) {
+cudaError_t launch_rs_walk(const medusa_cfg& c, const TreeShape& ts, int ncta, int slice, const int32_t* tokens,
+                           const int32_t* first_child, const void* tl, const float* hl, const float2* stats,
+                           const float* ua, const float* ur, const WalkOut& w, cudaStream_t st) {
   if (C >= 8 && c.V % 8 == 0)
-    return launch_rs_walk_v<T, C, (C >= 8)>(c, ts, tokens, first_child, tl, hl, stats, ua, ur, w, st);
-  return launch_rs_walk_v<T, C, false>(c, ts, tokens, first_child, tl, hl, stats, ua, ur, w, st);
+    return launch_rs_walk_v<T, C, (C >= 8)>(c, ts, ncta, slice, tokens, first_child, tl, hl, stats, ua, ur, w, st);
+  return launch_rs_walk_v<T, C, false>(c, ts, ncta, slice, tokens, first_child, tl, hl, stats, ua, ur, w, st);
+}
+
+// CTAs per sequence: the largest power of two (at most 8) that keeps the whole
+// grid within two (256-thread) CTAs per SM.
+int rs_cluster_ctas(int B) {
+  int n = 1;
+  while (n < kMaxCluster && (long)B * n * 2 <= 2 * 152) n *= 2;
+  return n;
 }
 
 template <typename T>
@@ -679,13 +908,17 @@ cudaError_t run_rs(const medusa_cfg& c, const TreeShape& ts, const int32_t* toke
   note_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int need = (c.V + kVThreads - 1) / kVThreads;
-  if (need <= 1) return launch_rs_walk<T, 1>(c, ts, tokens, first_child, tl, hl, stats, ua, ur, w, st);
-  if (need <= 2) return launch_rs_walk<T, 2>(c, ts, tokens, first_child, tl, hl, stats, ua, ur, w, st);
-  if (need <= 4) return launch_rs_walk<T, 4>(c, ts, tokens, first_child, tl, hl, stats, ua, ur, w, st);
-  if (need <= 8) return launch_rs_walk<T, 8>(c, ts, tokens, first_child, tl, hl, stats, ua, ur, w, st);
-  if (need <= 16) return launch_rs_walk<T, 16>(c, ts, tokens, first_child, tl, hl, stats, ua, ur, w, st);
-  return launch_rs_walk<T, 32>(c, ts, tokens, first_child, tl, hl, stats, ua, ur, w, st);
+  const int ncta = rs_cluster_ctas(c.B);
+  const int slice = (((c.V + ncta - 1) / ncta) + 7) / 8 * 8;
+  const int need = (slice + kVThreads - 1) / kVThreads;
+#define MEDUSA_RS(CC) return launch_rs_walk<T, CC>(c, ts, ncta, slice, tokens, first_child, tl, hl, stats, ua, ur, w, st)
+  if (need <= 1) MEDUSA_RS(1);
+  if (need <= 2) MEDUSA_RS(2);
+  if (need <= 4) MEDUSA_RS(4);
+  if (need <= 8) MEDUSA_RS(8);
+  if (need <= 16) MEDUSA_RS(16);
+  MEDUSA_RS(32);
+#undef MEDUSA_RS
 }
 
 template <typename T>
