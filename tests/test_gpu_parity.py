@@ -255,6 +255,31 @@ def test_verify_rejection_decisions(name, T):
     assert total_acc > 0
 
 
+# The walk runs on a cluster of 8 / 4 / 2 / 1 CTAs per sequence depending on B
+# (at most two 256-thread CTAs per SM); vocabulary slices of unequal length, rows
+# read 8 entries at a time or one at a time (V % 8 != 0).
+@pytest.mark.parametrize("B,V", [(8, 1000), (40, 4096), (80, 3001), (160, 2048)])
+def test_verify_rejection_cluster_sizes(B, V):
+    dev = gpu_ready()
+    w = configs.scaled(configs.get("gqa7b_b32"), B=B, V=V, temperature=0.9, L_range=(16, 64))
+    L, L_cap, root, topk, tree, tl, z, u_acc, u_res = rs_case(w, dev, seed=3)
+    st = DeviceStep(w, REJECTION, L_cap, dev)
+    st.tree_build(torch.from_numpy(root).to(dev), torch.from_numpy(L).to(dev), topk=torch.from_numpy(topk).to(dev))
+    st.verify(tl, torch.from_numpy(u_acc).to(dev), torch.from_numpy(u_res).to(dev), head_logits=z)
+    torch.cuda.synchronize()
+    ref = O.verify_batch(REJECTION, tree, f64(tl), w.K, head_logits=f64(z), u_acc=u_acc, u_res=u_res, T=w.temperature)
+    gflags = i64(st.flags)
+    compared = 0
+    for b in range(w.B):
+        if ref["flags"][b] or gflags[b]:
+            assert 1 <= int(st.n_out[b]) <= w.K + 1
+            continue
+        compared += 1
+        for key in ("acc", "path", "out_tokens", "n_out"):
+            assert np.array_equal(i64(getattr(st, key))[b], ref[key][b]), (key, b)
+    assert compared >= w.B // 2
+
+
 # --------------------------------------------------------------------------- compaction
 @pytest.mark.parametrize("name", NAMES)
 def test_kv_compact_bit_exact(name):
