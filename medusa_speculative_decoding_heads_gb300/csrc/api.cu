@@ -76,7 +76,7 @@ int medusa_heads(const medusa_cfg* cfg, const void* h, const void* W, const void
   if (!logits && cfg->mode == MEDUSA_REJECTION) return MEDUSA_ERR_INVALID_ARG;
   if (cfg->dtype == MEDUSA_BF16) {
     if (cfg->d % 64 != 0 || cfg->B > 32) return MEDUSA_ERR_UNSUPPORTED;
-    if (!aligned16(h) || !aligned16(W) || !aligned16(U)) return MEDUSA_ERR_INVALID_ARG;
+    if (!aligned16(h) || !aligned16(W) || !aligned16(U) || (bias && !aligned16(bias))) return MEDUSA_ERR_INVALID_ARG;
   }
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MEDUSA_ERR_INVALID_ARG;
   return from_cuda(launch_heads(*cfg, h, W, bias, U, logits, topk, workspace, (cudaStream_t)stream));

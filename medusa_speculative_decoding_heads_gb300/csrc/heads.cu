@@ -390,30 +390,92 @@ __device__ __forceinline__ void list_insert(float* lv, int* li, float x, int v) 
   }
 }
 
-// grid (P, K, B): slice p of row (b, k) -> s candidates at cand[((b*K + k)*P + p)*s_max + r].
-__global__ void __launch_bounds__(kTopThreads)
-topk_partial_kernel(const float* __restrict__ z, int V, TreeShape ts, int chunk, float* __restrict__ cv,
-                    int* __restrict__ ci) {
-  const int p = blockIdx.x, k = blockIdx.y, b = blockIdx.z, P = gridDim.x;
-  const int K = ts.K, s = ts.s[k + 1], s_max = ts.s_max;
-  const float* row = z + ((size_t)b * K + k) * V;
-  const int v0 = p * chunk, v1 = min(V, v0 + chunk);
-  float lv[kMaxS];
-  int li[kMaxS];
+// The s best of a lane's (value, index) list, kept sorted; S = the list length.
+template <int S>
+__device__ __forceinline__ void list_insert_s(float* lv, int* li, float x, int v) {
+  if (!better(x, v, lv[S - 1], li[S - 1])) return;
+  float cv = x;
+  int ci = v;
 #pragma unroll
-  for (int i = 0; i < kMaxS; ++i) {
+  for (int k = 0; k < S; ++k) {
+    if (better(cv, ci, lv[k], li[k])) {
+      const float tv = lv[k];
+      const int ti = li[k];
+      lv[k] = cv;
+      li[k] = ci;
+      cv = tv;
+      ci = ti;
+    }
+  }
+}
+
+// Pops the S best of the lanes' sorted lists in order.
+template <int S>
+__device__ __forceinline__ void warp_top_s_t(float* lv, int* li, float* ov, int* oi) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < S; ++r) {
+    float v = lv[0];
+    int i = li[0];
+    int who = lane;
+    warp_best(v, i, who);
+    ov[r] = v;
+    oi[r] = i;
+    if (lane == who) {
+#pragma unroll
+      for (int k = 0; k < S - 1; ++k) {
+        lv[k] = lv[k + 1];
+        li[k] = li[k + 1];
+      }
+      lv[S - 1] = -INFINITY;
+      li[S - 1] = 0x7fffffff;
+    }
+  }
+}
+
+// One CTA: the S best of row[v0, v1). With VEC4 (rows and slices aligned to 4
+// floats) every thread issues two 16-byte loads per step before inserting.
+template <int S, bool VEC4>
+__device__ __forceinline__ void topk_slice(const float* __restrict__ row, int v0, int v1, float* __restrict__ out_v,
+                                           int* __restrict__ out_i) {
+  float lv[S];
+  int li[S];
+#pragma unroll
+  for (int i = 0; i < S; ++i) {
     lv[i] = -INFINITY;
     li[i] = 0x7fffffff;
   }
-  for (int v = v0 + threadIdx.x; v < v1; v += kTopThreads) list_insert(lv, li, row[v], v);
+  if (VEC4) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    const int g0 = v0 >> 2, g1 = v1 >> 2;
+    for (int g = g0 + threadIdx.x; g < g1; g += 2 * kTopThreads) {
+      const float4 a = r4[g];
+      const bool two = g + kTopThreads < g1;
+      const float4 c = two ? r4[g + kTopThreads] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      list_insert_s<S>(lv, li, a.x, 4 * g);
+      list_insert_s<S>(lv, li, a.y, 4 * g + 1);
+      list_insert_s<S>(lv, li, a.z, 4 * g + 2);
+      list_insert_s<S>(lv, li, a.w, 4 * g + 3);
+      if (two) {
+        const int gc = g + kTopThreads;
+        list_insert_s<S>(lv, li, c.x, 4 * gc);
+        list_insert_s<S>(lv, li, c.y, 4 * gc + 1);
+        list_insert_s<S>(lv, li, c.z, 4 * gc + 2);
+        list_insert_s<S>(lv, li, c.w, 4 * gc + 3);
+      }
+    }
+  } else {
+    for (int v = v0 + threadIdx.x; v < v1; v += kTopThreads) list_insert_s<S>(lv, li, row[v], v);
+  }
   __shared__ float wv[kTopThreads / 32][kMaxS];
   __shared__ int wi[kTopThreads / 32][kMaxS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float tv[kMaxS];
-  int ti[kMaxS];
-  warp_top_s(lv, li, s, tv, ti);
+  float tv[S];
+  int ti[S];
+  warp_top_s_t<S>(lv, li, tv, ti);
   if (lane == 0)
-    for (int r = 0; r < s; ++r) {
+#pragma unroll
+    for (int r = 0; r < S; ++r) {
       wv[warp][r] = tv[r];
       wi[warp][r] = ti[r];
     }
@@ -421,19 +483,40 @@ topk_partial_kernel(const float* __restrict__ z, int V, TreeShape ts, int chunk,
   if (warp == 0) {
     // lane w < 8 holds warp w's sorted list
 #pragma unroll
-    for (int i = 0; i < kMaxS; ++i) {
-      const bool have = lane < kTopThreads / 32 && i < s;
+    for (int i = 0; i < S; ++i) {
+      const bool have = lane < kTopThreads / 32;
       lv[i] = have ? wv[lane][i] : -INFINITY;
       li[i] = have ? wi[lane][i] : 0x7fffffff;
     }
-    warp_top_s(lv, li, s, tv, ti);
-    if (lane == 0) {
-      const size_t o = (((size_t)b * K + k) * P + p) * s_max;
-      for (int r = 0; r < s; ++r) {
-        cv[o + r] = tv[r];
-        ci[o + r] = ti[r];
+    warp_top_s_t<S>(lv, li, tv, ti);
+    if (lane == 0)
+#pragma unroll
+      for (int r = 0; r < S; ++r) {
+        out_v[r] = tv[r];
+        out_i[r] = ti[r];
       }
-    }
+  }
+}
+
+// grid (P, K, B): slice p of row (b, k) -> s candidates at cand[((b*K + k)*P + p)*s_max + r].
+template <bool VEC4>
+__global__ void __launch_bounds__(kTopThreads)
+topk_partial_kernel(const float* __restrict__ z, int V, TreeShape ts, int chunk, float* __restrict__ cv,
+                    int* __restrict__ ci) {
+  const int p = blockIdx.x, k = blockIdx.y, b = blockIdx.z, P = gridDim.x;
+  const int K = ts.K, s = ts.s[k + 1], s_max = ts.s_max;
+  const float* row = z + ((size_t)b * K + k) * V;
+  const int v0 = min(V, p * chunk), v1 = min(V, v0 + chunk);
+  const size_t o = (((size_t)b * K + k) * P + p) * s_max;
+  switch (s) {
+    case 1: topk_slice<1, VEC4>(row, v0, v1, cv + o, ci + o); break;
+    case 2: topk_slice<2, VEC4>(row, v0, v1, cv + o, ci + o); break;
+    case 3: topk_slice<3, VEC4>(row, v0, v1, cv + o, ci + o); break;
+    case 4: topk_slice<4, VEC4>(row, v0, v1, cv + o, ci + o); break;
+    case 5: topk_slice<5, VEC4>(row, v0, v1, cv + o, ci + o); break;
+    case 6: topk_slice<6, VEC4>(row, v0, v1, cv + o, ci + o); break;
+    case 7: topk_slice<7, VEC4>(row, v0, v1, cv + o, ci + o); break;
+    default: topk_slice<8, VEC4>(row, v0, v1, cv + o, ci + o); break;
   }
 }
 
@@ -558,10 +641,14 @@ cudaError_t launch_heads(const medusa_cfg& c, const void* h, const void* W, cons
   }
   const TreeShape ts = tree_shape(c);
   const int P = topk_slices(c);
-  const int chunk = (V + P - 1) / P;
+  const bool vec4 = V % 4 == 0 && (reinterpret_cast<uintptr_t>(z) & 15u) == 0;
+  const int chunk = vec4 ? ((V + P - 1) / P + 3) / 4 * 4 : (V + P - 1) / P;
   float* cv = reinterpret_cast<float*>(base + p.cand);
   int* ci = reinterpret_cast<int*>(cv + (size_t)B * K * P * kMaxS);
-  topk_partial_kernel<<<dim3(P, K, B), kTopThreads, 0, st>>>(z, V, ts, chunk, cv, ci);
+  if (vec4)
+    topk_partial_kernel<true><<<dim3(P, K, B), kTopThreads, 0, st>>>(z, V, ts, chunk, cv, ci);
+  else
+    topk_partial_kernel<false><<<dim3(P, K, B), kTopThreads, 0, st>>>(z, V, ts, chunk, cv, ci);
   note_launches(1);
   topk_merge_kernel<<<dim3(K, B), 32, 0, st>>>(cv, ci, P, ts, topk);
   note_launches(1);

@@ -195,24 +195,45 @@ __global__ void pack_h_tc_kernel(const uint16_t* __restrict__ h, uint16_t* __res
 __global__ void residual_pack_tc_kernel(const float* __restrict__ part, int ksplit, const uint16_t* __restrict__ h,
                                         const uint16_t* __restrict__ bias, uint16_t* __restrict__ X2, int B, int NB,
                                         int K, int d) {
-  const size_t total = (size_t)K * NB * d;
+  // four consecutive outputs o per thread: 16-byte partial loads, 8-byte stores
+  const int d4 = d >> 2;
+  const size_t total = (size_t)K * NB * d4;
   const size_t split_stride = (size_t)B * K * d;
   for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
-    const int o = (int)(e % d);
-    const int n = (int)((e / d) % NB);
-    const int k = (int)(e / ((size_t)d * NB));
-    uint16_t hi = 0, lo = 0;
+    const int o = (int)(e % d4) * 4;
+    const int n = (int)((e / d4) % NB);
+    const int k = (int)(e / ((size_t)d4 * NB));
+    uint32_t hi2[2] = {0u, 0u}, lo2[2] = {0u, 0u};
     if (n < B) {
-      float pre = 0.f;
-      for (int s = 0; s < ksplit; ++s) pre += part[s * split_stride + ((size_t)n * K + k) * d + o];
-      if (bias) pre += bf16_to_f32(bias[(size_t)k * d + o]);
-      const float r = bf16_to_f32(h[(size_t)n * d + o]) + pre / (1.f + expf(-pre));
-      hi = f32_to_bf16(r);
-      lo = f32_to_bf16(r - bf16_to_f32(hi));
+      float pre[4] = {0.f, 0.f, 0.f, 0.f};
+      const float* pp = part + ((size_t)n * K + k) * d + o;
+      for (int s = 0; s < ksplit; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(pp + s * split_stride);
+        pre[0] += v.x;
+        pre[1] += v.y;
+        pre[2] += v.z;
+        pre[3] += v.w;
+      }
+      const uint2 hv = *reinterpret_cast<const uint2*>(h + (size_t)n * d + o);
+      uint2 bv = make_uint2(0u, 0u);
+      if (bias) bv = *reinterpret_cast<const uint2*>(bias + (size_t)k * d + o);
+      const uint32_t hw[2] = {hv.x, hv.y}, bw[2] = {bv.x, bv.y};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint16_t hq = (uint16_t)(hw[q >> 1] >> (16 * (q & 1)));
+        const uint16_t bq = (uint16_t)(bw[q >> 1] >> (16 * (q & 1)));
+        float x = pre[q];
+        if (bias) x += bf16_to_f32(bq);
+        const float r = bf16_to_f32(hq) + x / (1.f + expf(-x));
+        const uint16_t rh = f32_to_bf16(r);
+        const uint16_t rl = f32_to_bf16(r - bf16_to_f32(rh));
+        hi2[q >> 1] |= (uint32_t)rh << (16 * (q & 1));
+        lo2[q >> 1] |= (uint32_t)rl << (16 * (q & 1));
+      }
     }
     uint16_t* xk = X2 + (size_t)k * 2 * NB * d;
-    xk[(size_t)n * d + o] = hi;
-    xk[(size_t)(NB + n) * d + o] = lo;
+    *reinterpret_cast<uint2*>(xk + (size_t)n * d + o) = make_uint2(hi2[0], hi2[1]);
+    *reinterpret_cast<uint2*>(xk + (size_t)(NB + n) * d + o) = make_uint2(lo2[0], lo2[1]);
   }
 }
 
@@ -294,7 +315,8 @@ cudaError_t launch_heads_tc(const medusa_cfg& c, const void* h, const void* W, c
                       ? run_gemv<16, false>(tmW, tmX1, d, K, 0, nchunks, p.ksplit1, B, part1, (size_t)B * K * d, sms, st)
                       : run_gemv<32, false>(tmW, tmX1, d, K, 0, nchunks, p.ksplit1, B, part1, (size_t)B * K * d, sms, st);
   if (e != cudaSuccess) return e;
-  residual_pack_tc_kernel<<<512, 256, 0, st>>>(part1, p.ksplit1, static_cast<const uint16_t*>(h),
+  const int rp_blocks = (int)(((size_t)K * p.NB * (d / 4) + 255) / 256);
+  residual_pack_tc_kernel<<<rp_blocks < 1024 ? rp_blocks : 1024, 256, 0, st>>>(part1, p.ksplit1, static_cast<const uint16_t*>(h),
                                                static_cast<const uint16_t*>(bias), x2, B, p.NB, K, d);
   note_launches(1);
   switch (p.NCOL2) {
