@@ -79,7 +79,7 @@ size_t heads_workspace(const medusa_cfg& c);
 // Tensor-core (tcgen05) heads path.
 struct HeadsTcPlan {
   int NB, NCOL1, NCOL2, ksplit1;
-  size_t x1, x2, part1, total;
+  size_t x2, part1, total;
 };
 HeadsTcPlan plan_heads_tc(const medusa_cfg& c);
 bool heads_tc_supported(const medusa_cfg& c);

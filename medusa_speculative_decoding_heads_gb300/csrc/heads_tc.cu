@@ -179,18 +179,6 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   }
 }
 
-// X1[n][i] = h[n][i] (bf16) for n < B, zero rows up to NCOL1.
-__global__ void pack_h_tc_kernel(const uint16_t* __restrict__ h, uint16_t* __restrict__ X1, int B, int NCOL1, int d) {
-  const size_t total = (size_t)NCOL1 * d / 8;
-  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < total; v += (size_t)gridDim.x * blockDim.x) {
-    const int n = (int)(v * 8 / d);
-    const int i = (int)(v * 8 % d);
-    uint4 x = make_uint4(0, 0, 0, 0);
-    if (n < B) x = *reinterpret_cast<const uint4*>(h + (size_t)n * d + i);
-    *reinterpret_cast<uint4*>(X1 + v * 8) = x;
-  }
-}
-
 // r = h + SiLU(sum_splits pre + bias); X2[k][n][o] = bf16(r), X2[k][NB+n][o] = bf16(r - bf16(r)).
 __global__ void residual_pack_tc_kernel(const float* __restrict__ part, int ksplit, const uint16_t* __restrict__ h,
                                         const uint16_t* __restrict__ bias, uint16_t* __restrict__ X2, int B, int NB,
@@ -284,7 +272,6 @@ HeadsTcPlan plan_heads_tc(const medusa_cfg& c) {
     off = align_up(off + bytes, 256);
     return o;
   };
-  p.x1 = take((size_t)p.NCOL1 * c.d * 2);
   p.x2 = take((size_t)c.K * p.NCOL2 * c.d * 2);
   p.part1 = take((size_t)p.ksplit1 * c.B * c.K * c.d * 4);
   p.total = off;
@@ -296,21 +283,20 @@ bool heads_tc_supported(const medusa_cfg& c) { return c.dtype == MEDUSA_BF16 && 
 cudaError_t launch_heads_tc(const medusa_cfg& c, const void* h, const void* W, const void* bias, const void* U,
                             float* z, char* ws, cudaStream_t st) {
   const HeadsTcPlan p = plan_heads_tc(c);
-  uint16_t* x1 = reinterpret_cast<uint16_t*>(ws + p.x1);
   uint16_t* x2 = reinterpret_cast<uint16_t*>(ws + p.x2);
   float* part1 = reinterpret_cast<float*>(ws + p.part1);
   const int B = c.B, d = c.d, V = c.V, K = c.K;
   const int nchunks = d / kChunkK;
   CUtensorMap tmW, tmX1, tmU, tmX2;
   if (!encode_tmap_2d_bf16(&tmW, W, (uint64_t)K * d, d, (uint64_t)d * 2, kChunkK, kRowsTile) ||
-      !encode_tmap_2d_bf16(&tmX1, x1, p.NCOL1, d, (uint64_t)d * 2, kChunkK, p.NCOL1) ||
+      // the residual layer reads h itself: rows B..NCOL1-1 of each box lie past
+      // the tensor and arrive as zeros
+      !encode_tmap_2d_bf16(&tmX1, h, (uint64_t)B, d, (uint64_t)d * 2, kChunkK, p.NCOL1) ||
       !encode_tmap_2d_bf16(&tmU, U, (uint64_t)K * V, d, (uint64_t)d * 2, kChunkK, kRowsTile) ||
       !encode_tmap_2d_bf16(&tmX2, x2, (uint64_t)K * p.NCOL2, d, (uint64_t)d * 2, kChunkK, p.NCOL2))
     return cudaErrorInvalidValue;
   const int sms = sm_count();
 
-  pack_h_tc_kernel<<<64, 256, 0, st>>>(static_cast<const uint16_t*>(h), x1, B, p.NCOL1, d);
-  note_launches(1);
   cudaError_t e = p.NCOL1 == 16
                       ? run_gemv<16, false>(tmW, tmX1, d, K, 0, nchunks, p.ksplit1, B, part1, (size_t)B * K * d, sms, st)
                       : run_gemv<32, false>(tmW, tmX1, d, K, 0, nchunks, p.ksplit1, B, part1, (size_t)B * K * d, sms, st);
