@@ -84,6 +84,8 @@ tree_attn_partial_kernel(const T* __restrict__ Q, const T* __restrict__ Kc, cons
                          const int32_t* __restrict__ L, const uint64_t* __restrict__ bits, int N, int Hq, int Hkv,
                          int L_cap, int chunk, float scale_log2, float* __restrict__ o_part,
                          float* __restrict__ ml_part) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int DPL = D / 32;   // head-dim values per lane
   __shared__ float qs[kRowsPerCta][D];
   __shared__ float ks[kKeyTile][D + 1];
@@ -196,6 +198,8 @@ template <typename T, int D>
 __global__ void tree_attn_merge_kernel(const float* __restrict__ o_part, const float* __restrict__ ml_part, int B,
                                        int N, int Hq, int nsplit, const int32_t* __restrict__ L, int L_cap,
                                        T* __restrict__ O) {
+  pdl_wait();
+  pdl_trigger();
   const size_t rows = (size_t)B * N * Hq;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -247,7 +251,7 @@ cudaError_t run(const medusa_cfg& c, const AttnPlan& p, const void* Q, const voi
   } else {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
     dim3 grid(p.row_groups, c.Hkv * c.B, p.nsplit);
-    tree_attn_partial_kernel<T, D><<<grid, kAttnWarps * 32, 0, st>>>(
+    launch_pdl(tree_attn_partial_kernel<T, D>, grid, kAttnWarps * 32, 0, st, 
         static_cast<const T*>(Q), static_cast<const T*>(Kc), static_cast<const T*>(Vc), L, bits, ts.N, c.Hq, c.Hkv,
         c.L_cap, p.chunk, scale_log2, o_part, ml_part);
     note_launches(1);
@@ -255,7 +259,7 @@ cudaError_t run(const medusa_cfg& c, const AttnPlan& p, const void* Q, const voi
   }
   if (e != cudaSuccess) return e;
   const size_t rows = (size_t)c.B * ts.N * c.Hq;
-  tree_attn_merge_kernel<T, D><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(
+  launch_pdl(tree_attn_merge_kernel<T, D>, (unsigned)((rows * 32 + 255) / 256), 256, 0, st, 
       o_part, ml_part, c.B, ts.N, c.Hq, p.nsplit, L, c.L_cap, static_cast<T*>(O));
   note_launches(1);
   return cudaGetLastError();

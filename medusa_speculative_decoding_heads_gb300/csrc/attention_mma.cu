@@ -75,6 +75,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
 tree_attn_mma_kernel(const uint16_t* __restrict__ Q, const uint16_t* __restrict__ Kc, const uint16_t* __restrict__ Vc,
                      const int32_t* __restrict__ L, const uint64_t* __restrict__ bits, int N, int Hq, int Hkv,
                      int L_cap, int chunk, float scale_log2, float* __restrict__ o_part, float* __restrict__ ml_part) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int KS = D / 16;        // k-steps of Q K^T
   constexpr int NT = D / 8;         // n-tiles of P V
   constexpr int CH = D / 8;         // 16-byte chunks per row
@@ -315,14 +317,14 @@ cudaError_t launch_attention_mma(const medusa_cfg& c, int nsplit, int chunk, con
     const size_t smem = 2 * kStages * kKeys * 128 * 2;
     e = cudaFuncSetAttribute(tree_attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    tree_attn_mma_kernel<128><<<grid, warps * 32, smem, st>>>(
+    launch_pdl(tree_attn_mma_kernel<128>, grid, warps * 32, smem, st, 
         static_cast<const uint16_t*>(Q), static_cast<const uint16_t*>(Kc), static_cast<const uint16_t*>(Vc), L, bits,
         ts.N, c.Hq, c.Hkv, c.L_cap, chunk, scale_log2, o_part, ml_part);
   } else {
     const size_t smem = 2 * kStages * kKeys * 64 * 2;
     e = cudaFuncSetAttribute(tree_attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    tree_attn_mma_kernel<64><<<grid, warps * 32, smem, st>>>(
+    launch_pdl(tree_attn_mma_kernel<64>, grid, warps * 32, smem, st, 
         static_cast<const uint16_t*>(Q), static_cast<const uint16_t*>(Kc), static_cast<const uint16_t*>(Vc), L, bits,
         ts.N, c.Hq, c.Hkv, c.L_cap, chunk, scale_log2, o_part, ml_part);
   }

@@ -138,6 +138,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     const uint16_t* __restrict__ Q, const int32_t* __restrict__ L, const uint64_t* __restrict__ bits,
                     int N, int Hq, int Hkv, int L_cap, int chunk, float scale_log2, float* __restrict__ o_part,
                     float* __restrict__ ml_part, uint16_t* __restrict__ O) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = sm;                                                    // [stage][K | V]
@@ -491,7 +493,7 @@ cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, cons
   const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)kD));
   const int NG = ts.N * (c.Hq / c.Hkv);
   dim3 grid(attention_tc_mtiles(NG), c.Hkv * c.B, nsplit);
-  tree_attn_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmK, tmV, static_cast<const uint16_t*>(Q), L, bits, ts.N, c.Hq,
+  launch_pdl(tree_attn_tc_kernel, grid, kThreads, kSmemBytes, st, tmK, tmV, static_cast<const uint16_t*>(Q), L, bits, ts.N, c.Hq,
                                                      c.Hkv, c.L_cap, chunk, scale_log2, o_part, ml_part,
                                                      static_cast<uint16_t*>(O));
   note_launches(1);

@@ -8,6 +8,30 @@
 
 namespace medusa {
 
+// Programmatic dependent launch. Every kernel of the library is launched with
+// programmatic stream serialization, so it may start while the previous kernel
+// on the stream is still finishing; pdl_wait() blocks until that kernel has
+// completed and its memory is visible, and must precede every access to global
+// memory that another kernel wrote or will read. pdl_trigger() lets the next
+// kernel launch as soon as every CTA of this one has started.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 constexpr int kMaxK = 8;
 constexpr int kMaxS = 8;
 constexpr int kMaxN = 128;

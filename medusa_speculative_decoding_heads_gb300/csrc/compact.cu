@@ -26,6 +26,8 @@ __device__ __forceinline__ bool valid_walk(int Lb, int N, int L_cap, int a, int 
 __global__ void __launch_bounds__(64)
 kv_compact_kernel(uint4* __restrict__ Kc, uint4* __restrict__ Vc, int row_vec, int L_cap, int N, int K,
                   const int32_t* __restrict__ L, const int32_t* __restrict__ acc, const int32_t* __restrict__ path) {
+  pdl_wait();
+  pdl_trigger();
   const int h = blockIdx.x, b = blockIdx.y, Hkv = gridDim.x;
   const int Lb = L[b];
   const int a = acc[b];
@@ -51,6 +53,8 @@ kv_compact_kernel(uint4* __restrict__ Kc, uint4* __restrict__ Vc, int row_vec, i
 
 __global__ void kv_finish_kernel(int B, int N, int K, int L_cap, int32_t* __restrict__ L, const int32_t* __restrict__ acc,
                                  const int32_t* __restrict__ path, int32_t* __restrict__ kv_map) {
+  pdl_wait();
+  pdl_trigger();
   for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
     const int Lb = L[b];
     const int a = acc[b];
@@ -67,12 +71,12 @@ cudaError_t launch_kv_compact(const medusa_cfg& c, void* Kc, void* Vc, int32_t* 
   const TreeShape ts = tree_shape(c);
   const int elt = c.dtype == MEDUSA_F32 ? 4 : 2;
   const int row_vec = c.D * elt / 16;
-  kv_compact_kernel<<<dim3(c.Hkv, c.B), 64, 0, st>>>(static_cast<uint4*>(Kc), static_cast<uint4*>(Vc), row_vec,
+  launch_pdl(kv_compact_kernel, dim3(c.Hkv, c.B), 64, 0, st, static_cast<uint4*>(Kc), static_cast<uint4*>(Vc), row_vec,
                                                       c.L_cap, ts.N, c.K, L, acc, path);
   note_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  kv_finish_kernel<<<(c.B + 127) / 128, 128, 0, st>>>(c.B, ts.N, c.K, c.L_cap, L, acc, path, kv_map);
+  launch_pdl(kv_finish_kernel, (c.B + 127) / 128, 128, 0, st, c.B, ts.N, c.K, c.L_cap, L, acc, path, kv_map);
   note_launches(1);
   return cudaGetLastError();
 }

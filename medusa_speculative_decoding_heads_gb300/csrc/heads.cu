@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 heads_mma_kernel(const uint16_t* __restrict__ A, size_t a_group_stride, int rows, int d,
                  const uint16_t* __restrict__ Xp, size_t xp_group_stride, int chunks_per_split,
                  float* __restrict__ out, size_t out_split_stride, int B, int G) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ __align__(16) uint16_t xs[kXStages][NT * P * 2 * 256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, cq = lane & 3;
@@ -200,6 +202,8 @@ heads_mma_kernel(const uint16_t* __restrict__ A, size_t a_group_stride, int rows
 // Pack the bf16 hidden state into the vector-operand layout (hi part only).
 template <int NT>
 __global__ void pack_h_kernel(const uint16_t* __restrict__ h, uint16_t* __restrict__ Xp, int B, int d) {
+  pdl_wait();
+  pdl_trigger();
   const int nchunks = d / kChunk;
   const size_t total = (size_t)nchunks * NT * 2 * 32;   // (c, t, hh, lane) vectors of 8
   for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < total; v += (size_t)gridDim.x * blockDim.x) {
@@ -221,6 +225,8 @@ template <int NT>
 __global__ void residual_pack_kernel(const float* __restrict__ part, int ksplit, const uint16_t* __restrict__ h,
                                      const uint16_t* __restrict__ bias, uint16_t* __restrict__ Xp2, int B, int K,
                                      int d) {
+  pdl_wait();
+  pdl_trigger();
   const int nchunks = d / kChunk;
   const size_t total = (size_t)K * nchunks * NT * 2 * 32;   // (k, c, t, hh, lane)
   const size_t split_stride = (size_t)B * K * d;
@@ -272,6 +278,8 @@ __global__ void __launch_bounds__(256)
 heads_f32_kernel(const float* __restrict__ A, int rows, int d, const float* __restrict__ X, size_t x_b_stride,
                  size_t x_group_stride, int B, int G, float* __restrict__ out, const float* __restrict__ h,
                  const float* __restrict__ bias) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float xs[kF32B][kF32DChunk];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y;
@@ -503,6 +511,8 @@ template <bool VEC4>
 __global__ void __launch_bounds__(kTopThreads)
 topk_partial_kernel(const float* __restrict__ z, int V, TreeShape ts, int chunk, float* __restrict__ cv,
                     int* __restrict__ ci) {
+  pdl_wait();
+  pdl_trigger();
   const int p = blockIdx.x, k = blockIdx.y, b = blockIdx.z, P = gridDim.x;
   const int K = ts.K, s = ts.s[k + 1], s_max = ts.s_max;
   const float* row = z + ((size_t)b * K + k) * V;
@@ -523,6 +533,8 @@ topk_partial_kernel(const float* __restrict__ z, int V, TreeShape ts, int chunk,
 // grid (K, B), one warp: merge P slices' candidates into topk[b][k][:].
 __global__ void topk_merge_kernel(const float* __restrict__ cv, const int* __restrict__ ci, int P, TreeShape ts,
                                   int32_t* __restrict__ topk) {
+  pdl_wait();
+  pdl_trigger();
   const int k = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
   const int K = ts.K, s = ts.s[k + 1], s_max = ts.s_max;
   float lv[kMaxS];
@@ -614,12 +626,12 @@ cudaError_t launch_heads(const medusa_cfg& c, const void* h, const void* W, cons
     const size_t xp2_group = (size_t)nchunks * p.NT * 2 * 512;
 #define MEDUSA_HEADS_BF16(NT_)                                                                                   \
   do {                                                                                                           \
-    pack_h_kernel<NT_><<<64, 256, 0, st>>>(static_cast<const uint16_t*>(h), xp1, B, d);                           \
-    heads_mma_kernel<NT_, 1><<<g1, kWarps * 32, 0, st>>>(static_cast<const uint16_t*>(W), (size_t)d * d, d, d,   \
+    launch_pdl(pack_h_kernel<NT_>, 64, 256, 0, st, static_cast<const uint16_t*>(h), xp1, B, d);                           \
+    launch_pdl(heads_mma_kernel<NT_, 1>, g1, kWarps * 32, 0, st, static_cast<const uint16_t*>(W), (size_t)d * d, d, d,   \
                                                         xp1, 0, cps1, part1, (size_t)B * K * d, B, K);          \
-    residual_pack_kernel<NT_><<<256, 256, 0, st>>>(part1, p.ksplit1, static_cast<const uint16_t*>(h),           \
+    launch_pdl(residual_pack_kernel<NT_>, 256, 256, 0, st, part1, p.ksplit1, static_cast<const uint16_t*>(h),           \
                                                    static_cast<const uint16_t*>(bias), xp2, B, K, d);           \
-    heads_mma_kernel<NT_, 2><<<g2, kWarps * 32, 0, st>>>(static_cast<const uint16_t*>(U), (size_t)V * d, V, d,   \
+    launch_pdl(heads_mma_kernel<NT_, 2>, g2, kWarps * 32, 0, st, static_cast<const uint16_t*>(U), (size_t)V * d, V, d,   \
                                                         xp2, xp2_group, nchunks, z, 0, B, K);                   \
     note_launches(4);                                                                                            \
   } while (0)
@@ -630,12 +642,12 @@ cudaError_t launch_heads(const medusa_cfg& c, const void* h, const void* W, cons
   } else {
     float* r = reinterpret_cast<float*>(base + p.xp2);
     dim3 g1((d + 32 - 1) / 32, K);
-    heads_f32_kernel<true><<<g1, 256, 0, st>>>(static_cast<const float*>(W), d, d, static_cast<const float*>(h),
+    launch_pdl(heads_f32_kernel<true>, g1, 256, 0, st, static_cast<const float*>(W), d, d, static_cast<const float*>(h),
                                                (size_t)d, 0, B, K, r, static_cast<const float*>(h),
                                                static_cast<const float*>(bias));
     note_launches(1);
     dim3 g2((V + 32 - 1) / 32, K);
-    heads_f32_kernel<false><<<g2, 256, 0, st>>>(static_cast<const float*>(U), V, d, r, (size_t)K * d, (size_t)d, B,
+    launch_pdl(heads_f32_kernel<false>, g2, 256, 0, st, static_cast<const float*>(U), V, d, r, (size_t)K * d, (size_t)d, B,
                                                 K, z, nullptr, nullptr);
     note_launches(1);
   }
@@ -646,11 +658,11 @@ cudaError_t launch_heads(const medusa_cfg& c, const void* h, const void* W, cons
   float* cv = reinterpret_cast<float*>(base + p.cand);
   int* ci = reinterpret_cast<int*>(cv + (size_t)B * K * P * kMaxS);
   if (vec4)
-    topk_partial_kernel<true><<<dim3(P, K, B), kTopThreads, 0, st>>>(z, V, ts, chunk, cv, ci);
+    launch_pdl(topk_partial_kernel<true>, dim3(P, K, B), kTopThreads, 0, st, z, V, ts, chunk, cv, ci);
   else
-    topk_partial_kernel<false><<<dim3(P, K, B), kTopThreads, 0, st>>>(z, V, ts, chunk, cv, ci);
+    launch_pdl(topk_partial_kernel<false>, dim3(P, K, B), kTopThreads, 0, st, z, V, ts, chunk, cv, ci);
   note_launches(1);
-  topk_merge_kernel<<<dim3(K, B), 32, 0, st>>>(cv, ci, P, ts, topk);
+  launch_pdl(topk_merge_kernel, dim3(K, B), 32, 0, st, cv, ci, P, ts, topk);
   note_launches(1);
   return cudaGetLastError();
 }

@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(192, 1)
 heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmX, int rows, int G,
                 int x_rows, int nchunks, int nk, int ksplit, int B, float* __restrict__ out,
                 size_t out_split_stride) {
+  pdl_trigger();
   using Geo = HeadsGeom<NCOL>;
   constexpr int S = Geo::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -84,6 +85,7 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = tmem_slot;
+  pdl_wait();   // the setup above overlaps the previous kernel's tail; no global access before this
 
   if (warp == 4) {
     if (lane == 0) {
@@ -183,6 +185,8 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 __global__ void residual_pack_tc_kernel(const float* __restrict__ part, int ksplit, const uint16_t* __restrict__ h,
                                         const uint16_t* __restrict__ bias, uint16_t* __restrict__ X2, int B, int NB,
                                         int K, int d) {
+  pdl_wait();
+  pdl_trigger();
   // four consecutive outputs o per thread: 16-byte partial loads, 8-byte stores
   const int d4 = d >> 2;
   const size_t total = (size_t)K * NB * d4;
@@ -236,7 +240,7 @@ cudaError_t run_gemv(const CUtensorMap& tmA, const CUtensorMap& tmX, int rows, i
                                        Geo::kSmem);
   if (e != cudaSuccess) return e;
   const int grid = nunits < num_sms ? nunits : num_sms;
-  heads_tc_kernel<NCOL, HILO><<<grid, 192, Geo::kSmem, st>>>(tmA, tmX, rows, G, x_rows, nchunks, nk, ks, B, out,
+  launch_pdl(heads_tc_kernel<NCOL, HILO>, grid, 192, Geo::kSmem, st, tmA, tmX, rows, G, x_rows, nchunks, nk, ks, B, out,
                                                               out_split_stride);
   note_launches(1);
   return cudaGetLastError();
@@ -302,7 +306,7 @@ cudaError_t launch_heads_tc(const medusa_cfg& c, const void* h, const void* W, c
                       : run_gemv<32, false>(tmW, tmX1, d, K, 0, nchunks, p.ksplit1, B, part1, (size_t)B * K * d, sms, st);
   if (e != cudaSuccess) return e;
   const int rp_blocks = (int)(((size_t)K * p.NB * (d / 4) + 255) / 256);
-  residual_pack_tc_kernel<<<rp_blocks < 1024 ? rp_blocks : 1024, 256, 0, st>>>(part1, p.ksplit1, static_cast<const uint16_t*>(h),
+  launch_pdl(residual_pack_tc_kernel, rp_blocks < 1024 ? rp_blocks : 1024, 256, 0, st, part1, p.ksplit1, static_cast<const uint16_t*>(h),
                                                static_cast<const uint16_t*>(bias), x2, B, p.NB, K, d);
   note_launches(1);
   switch (p.NCOL2) {

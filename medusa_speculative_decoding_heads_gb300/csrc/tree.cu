@@ -35,6 +35,8 @@ tree_build_kernel(TreeShape ts, int B, int L_cap, const int32_t* __restrict__ ro
                   const int32_t* __restrict__ L, int32_t* __restrict__ parent, int32_t* __restrict__ depth,
                   int32_t* __restrict__ first_child, uint8_t* __restrict__ mask, uint64_t* __restrict__ bits,
                   int32_t* __restrict__ tokens, int32_t* __restrict__ pos, uint32_t* __restrict__ flags) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint64_t sb[kMaxN][2];
   const int b = blockIdx.x;
   const int n = threadIdx.x;
@@ -77,7 +79,7 @@ cudaError_t launch_tree_build(const medusa_cfg& c, const int32_t* root, const in
                               int32_t* parent, int32_t* depth, int32_t* first_child, uint8_t* mask, uint64_t* bits,
                               int32_t* tokens, int32_t* pos, uint32_t* flags, cudaStream_t st) {
   const TreeShape ts = tree_shape(c);
-  tree_build_kernel<<<c.B, kMaxN, 0, st>>>(ts, c.B, c.L_cap, root, topk, L, parent, depth, first_child, mask, bits,
+  launch_pdl(tree_build_kernel, c.B, kMaxN, 0, st, ts, c.B, c.L_cap, root, topk, L, parent, depth, first_child, mask, bits,
                                            tokens, pos, flags);
   note_launches(1);
   return cudaGetLastError();

@@ -192,6 +192,8 @@ constexpr int kRowWarps = kRowThreads / 32;
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kRowThreads)
 row_argmax_kernel(const T* __restrict__ tl, int N, int V, int32_t* __restrict__ amax) {
+  pdl_wait();
+  pdl_trigger();
   const int n = blockIdx.x, b = blockIdx.y;
   const T* row = tl + ((size_t)b * N + n) * V;
   float bv = -INFINITY;
@@ -283,6 +285,8 @@ __device__ __forceinline__ FF ff_add8(FF acc, const float* e) {
 template <bool VEC>
 __global__ void __launch_bounds__(kRowThreads)
 head_stats_kernel(const float* __restrict__ hl, int K, int V, float c, float2* __restrict__ stats) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ Scratch<kRowWarps> s;
   const int k = blockIdx.x, b = blockIdx.y;
   const float* row = hl + ((size_t)b * K + k) * V;
@@ -329,6 +333,8 @@ struct WalkOut {
 __global__ void greedy_walk_kernel(TreeShape ts, int B, const int32_t* __restrict__ tokens,
                                    const int32_t* __restrict__ first_child, const int32_t* __restrict__ amax,
                                    WalkOut w) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int N = ts.N, K = ts.K;
@@ -692,6 +698,8 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
                const int32_t* __restrict__ first_child, const T* __restrict__ tl, const float* __restrict__ hl,
                const float2* __restrict__ hstats, const float* __restrict__ u_acc, const float* __restrict__ u_res,
                WalkOut w) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ float buf[];   // inverse-CDF transpose, [C][kPad]
   __shared__ Scratch<kVWarps> s;
   __shared__ WalkState ws;
@@ -864,13 +872,15 @@ cudaError_t launch_rs_walk_v(const medusa_cfg& c, const TreeShape& ts, int ncta,
   cfg.blockDim = dim3(kVThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = ncta;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // as launch_pdl
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, ts, c.V, slice, c.temperature, tokens, first_child, static_cast<const T*>(tl), hl,
                          stats, ua, ur, w);
   note_launches(1);
@@ -902,9 +912,9 @@ cudaError_t run_rs(const medusa_cfg& c, const TreeShape& ts, const int32_t* toke
                    cudaStream_t st) {
   const float cs = 1.4426950408889634f / c.temperature;
   if (c.V % 8 == 0)
-    head_stats_kernel<true><<<dim3(ts.K, c.B), kRowThreads, 0, st>>>(hl, ts.K, c.V, cs, stats);
+    launch_pdl(head_stats_kernel<true>, dim3(ts.K, c.B), kRowThreads, 0, st, hl, ts.K, c.V, cs, stats);
   else
-    head_stats_kernel<false><<<dim3(ts.K, c.B), kRowThreads, 0, st>>>(hl, ts.K, c.V, cs, stats);
+    launch_pdl(head_stats_kernel<false>, dim3(ts.K, c.B), kRowThreads, 0, st, hl, ts.K, c.V, cs, stats);
   note_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -925,13 +935,13 @@ template <typename T>
 cudaError_t run_greedy(const medusa_cfg& c, const TreeShape& ts, const int32_t* tokens, const int32_t* first_child,
                        const void* tl, const WalkOut& w, int32_t* amax, cudaStream_t st) {
   if (c.V % 8 == 0)
-    row_argmax_kernel<T, true><<<dim3(ts.N, c.B), kRowThreads, 0, st>>>(static_cast<const T*>(tl), ts.N, c.V, amax);
+    launch_pdl(row_argmax_kernel<T, true>, dim3(ts.N, c.B), kRowThreads, 0, st, static_cast<const T*>(tl), ts.N, c.V, amax);
   else
-    row_argmax_kernel<T, false><<<dim3(ts.N, c.B), kRowThreads, 0, st>>>(static_cast<const T*>(tl), ts.N, c.V, amax);
+    launch_pdl(row_argmax_kernel<T, false>, dim3(ts.N, c.B), kRowThreads, 0, st, static_cast<const T*>(tl), ts.N, c.V, amax);
   note_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  greedy_walk_kernel<<<(c.B + 127) / 128, 128, 0, st>>>(ts, c.B, tokens, first_child, amax, w);
+  launch_pdl(greedy_walk_kernel, (c.B + 127) / 128, 128, 0, st, ts, c.B, tokens, first_child, amax, w);
   note_launches(1);
   return cudaGetLastError();
 }
