@@ -136,6 +136,20 @@ def algorithmic_bytes(w, L, acc, mode, with_bias=False):
             "total": heads + logits + kv + tree + out + visited}
 
 
+def replica_seed(seed, rank):
+    """Each replica draws its own inputs (weak scaling: fixed work per GPU)."""
+    return seed + 1000 * rank
+
+
+def replica_throughput(elapsed_ms, steps, world, device):
+    """Whole-job steps/s: every rank ran `steps` steps; the job time is the slowest rank's."""
+    if world > 1:
+        t = torch.tensor([float(elapsed_ms)], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    return elapsed_ms, world * steps / (elapsed_ms / 1000.0)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -294,7 +308,7 @@ def run_ours(args):
 
     w = configs.get(args.workload)
     mode = w.modes[0]
-    seed = args.seed + 1000 * rank
+    seed = replica_seed(args.seed, rank)
     si = synth.make_step_inputs(w, seed=seed, device=dev)
     tl = make_targets(w, si, dev, mode, seed)
     inp = to_device_inputs(si, tl, dev)
@@ -377,12 +391,8 @@ def run_ours(args):
     elapsed_ms = t0.elapsed_time(t1)
     per_call = {n: statistics.mean(m[i].elapsed_time(m[i + 1]) for m in marks) for i, n in enumerate(names)}
     heads_ms = per_call["heads"]
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms, value = replica_throughput(elapsed_ms, args.steps, world, dev)
     ms_per_step = elapsed_ms / args.steps
-    value = world * args.steps / (elapsed_ms / 1000.0)
 
     e2e = None if args.no_e2e else run_e2e(w, st, inp, L0, tl, si, args, stream, world)
 
@@ -504,12 +514,8 @@ def run_e2e(w, st, inp, L0, tl, si, args, stream, world):
             e2e_step()
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
-    if world > 1:
-        t = torch.tensor([ms], device=inp.h.device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": world * steps / (ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+    ms, e2e_value = replica_throughput(a.elapsed_time(b), steps, world, inp.h.device)
+    return {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps, "launch_mode": "cuda_graph" if graph else "eager"}
 
 
