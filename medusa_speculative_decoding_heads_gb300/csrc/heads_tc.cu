@@ -85,6 +85,17 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = tmem_slot;
+  if (warp == 4 && lane == 0) {
+    // Warm L2 with the weight boxes of this CTA's first S chunks while the
+    // previous kernel finishes (a prefetch is only a hint, so it cannot observe
+    // stale data; the real loads come after the wait below).
+    int n = 0;
+    for (int u = blockIdx.x; u < nunits && n < S; u += gridDim.x) {
+      const int ks = u % ksplit, t = (u / ksplit) % tiles, g = u / (ksplit * tiles);
+      const int c0 = ks * nk, c1 = min(nchunks, c0 + nk);
+      for (int c = c0; c < c1 && n < S; ++c, ++n) tc::tma_prefetch_2d(&tmA, c * kChunkK, g * rows + t * kRowsTile);
+    }
+  }
   pdl_wait();   // the setup above overlaps the previous kernel's tail; no global access before this
 
   if (warp == 4) {

@@ -70,6 +70,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Prefetch of one 2D TMA box into L2 (a cache hint: no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (canonical layouts of the
 // tcgen05 matrix descriptor: start >> 4 in bits 0-13, leading-dimension byte
 // offset >> 4 in 16-29, stride-dimension byte offset >> 4 in 32-45, descriptor
