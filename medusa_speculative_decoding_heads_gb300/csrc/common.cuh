@@ -102,7 +102,7 @@ size_t heads_workspace(const medusa_cfg& c);
 
 // Tensor-core (tcgen05) heads path.
 struct HeadsTcPlan {
-  int NB, NCOL1, NCOL2, ksplit1;
+  int NB, NCOL1, NCOL2, slots1;   // slots1: partial-sum slots of the residual layer
   size_t x2, part1, total;
 };
 HeadsTcPlan plan_heads_tc(const medusa_cfg& c);

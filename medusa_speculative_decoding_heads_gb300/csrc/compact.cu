@@ -8,8 +8,9 @@
 // For r = 0..acc_b: row L_b + r <- row L_b + path_r in every KV head, then
 // L_b += acc_b + 1. path is strictly increasing with path_r >= r (node ids at
 // depth r are at least r), so a destination r is never the source of a later
-// slot. Each lane owns one fixed 16-byte column slice of a row and loads every
-// source slice before storing any, so the in-place update needs no barrier.
+// slot. Each thread owns one 16-byte column slice of a (head, K or V) row set
+// and loads every source slice before storing any, so the in-place update
+// needs no barrier.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,45 +23,54 @@ __device__ __forceinline__ bool valid_walk(int Lb, int N, int L_cap, int a, int 
   return Lb >= 0 && Lb + N <= L_cap && a >= 0 && a <= K;
 }
 
-// grid (Hkv, B), block 64: warp 0 moves K rows, warp 1 moves V rows.
-__global__ void __launch_bounds__(64)
-kv_compact_kernel(uint4* __restrict__ Kc, uint4* __restrict__ Vc, int row_vec, int L_cap, int N, int K,
-                  const int32_t* __restrict__ L, const int32_t* __restrict__ acc, const int32_t* __restrict__ path) {
-  pdl_wait();
-  pdl_trigger();
-  const int h = blockIdx.x, b = blockIdx.y, Hkv = gridDim.x;
-  const int Lb = L[b];
-  const int a = acc[b];
-  if (!valid_walk(Lb, N, L_cap, a, K)) return;
-  uint4* base = (threadIdx.x < 32 ? Kc : Vc) + ((size_t)b * Hkv + h) * L_cap * row_vec;
-  const int32_t* pb = path + (size_t)b * (K + 1);
-  for (int col = threadIdx.x & 31; col < row_vec; col += 32) {
-    uint4 v[kMaxK + 1];
-#pragma unroll
-    for (int r = 0; r <= kMaxK; ++r) {
-      if (r > a) break;
-      int src = pb[r];
-      src = src < 0 ? 0 : (src >= N ? N - 1 : src);
-      v[r] = base[(size_t)(Lb + src) * row_vec + col];
-    }
-#pragma unroll
-    for (int r = 0; r <= kMaxK; ++r) {
-      if (r > a) break;
-      if (pb[r] != r) base[(size_t)(Lb + r) * row_vec + col] = v[r];
-    }
-  }
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__global__ void kv_finish_kernel(int B, int N, int K, int L_cap, int32_t* __restrict__ L, const int32_t* __restrict__ acc,
-                                 const int32_t* __restrict__ path, int32_t* __restrict__ kv_map) {
+constexpr int kCompactThreads = 256;
+constexpr int kCompactCluster = 8;   // CTAs per sequence (portable cluster size)
+
+// One cluster of ncta CTAs per sequence, grid (ncta, B): CTA r moves the K and
+// V rows of KV heads [r Hkv / ncta, (r + 1) Hkv / ncta), one 16-byte column
+// slice per thread and step. After a cluster barrier (so that every CTA has
+// read L[b]), CTA 0 writes the KV map and advances L[b].
+__global__ void __launch_bounds__(kCompactThreads)
+kv_compact_kernel(uint4* __restrict__ Kc, uint4* __restrict__ Vc, int Hkv, int row_vec, int L_cap, int N, int K,
+                  int32_t* __restrict__ L, const int32_t* __restrict__ acc, const int32_t* __restrict__ path,
+                  int32_t* __restrict__ kv_map) {
   pdl_wait();
   pdl_trigger();
-  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
-    const int Lb = L[b];
-    const int a = acc[b];
-    const bool ok = valid_walk(Lb, N, L_cap, a, K);
-    for (int r = 0; r <= K; ++r) kv_map[(size_t)b * (K + 1) + r] = (ok && r <= a) ? path[(size_t)b * (K + 1) + r] : -1;
-    if (ok) L[b] = Lb + a + 1;
+  const int rank = blockIdx.x, ncta = gridDim.x, b = blockIdx.y;
+  const int Lb = L[b];
+  const int a = acc[b];
+  const bool ok = valid_walk(Lb, N, L_cap, a, K);
+  const int32_t* pb = path + (size_t)b * (K + 1);
+  if (ok) {
+    int src[kMaxK + 1];
+#pragma unroll
+    for (int r = 0; r <= kMaxK; ++r) {
+      const int s = r <= a ? pb[r] : r;
+      src[r] = s < 0 ? 0 : (s >= N ? N - 1 : s);
+    }
+    const int h0 = rank * Hkv / ncta, h1 = (rank + 1) * Hkv / ncta;
+    const int items = (h1 - h0) * 2 * row_vec;   // (head, K or V, column)
+    for (int i = threadIdx.x; i < items; i += kCompactThreads) {
+      const int col = i % row_vec, hk = i / row_vec;
+      uint4* base = ((hk & 1) ? Vc : Kc) + ((size_t)b * Hkv + h0 + (hk >> 1)) * L_cap * row_vec + col;
+      uint4 v[kMaxK + 1];
+#pragma unroll
+      for (int r = 0; r <= kMaxK; ++r)
+        if (r <= a) v[r] = base[(size_t)(Lb + src[r]) * row_vec];
+#pragma unroll
+      for (int r = 0; r <= kMaxK; ++r)
+        if (r <= a && src[r] != r) base[(size_t)(Lb + r) * row_vec] = v[r];
+    }
+  }
+  cluster_barrier();
+  if (rank == 0) {
+    for (int r = threadIdx.x; r <= K; r += kCompactThreads)
+      kv_map[(size_t)b * (K + 1) + r] = (ok && r <= a) ? pb[r] : -1;
+    if (threadIdx.x == 0 && ok) L[b] = Lb + a + 1;
   }
 }
 
@@ -71,13 +81,25 @@ cudaError_t launch_kv_compact(const medusa_cfg& c, void* Kc, void* Vc, int32_t* 
   const TreeShape ts = tree_shape(c);
   const int elt = c.dtype == MEDUSA_F32 ? 4 : 2;
   const int row_vec = c.D * elt / 16;
-  launch_pdl(kv_compact_kernel, dim3(c.Hkv, c.B), 64, 0, st, static_cast<uint4*>(Kc), static_cast<uint4*>(Vc), row_vec,
-                                                      c.L_cap, ts.N, c.K, L, acc, path);
+  const int ncta = c.Hkv < kCompactCluster ? c.Hkv : kCompactCluster;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ncta, c.B);
+  cfg.blockDim = dim3(kCompactThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ncta;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // as launch_pdl
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kv_compact_kernel, static_cast<uint4*>(Kc), static_cast<uint4*>(Vc), c.Hkv,
+                                     row_vec, c.L_cap, ts.N, c.K, L, acc, path, kv_map);
   note_launches(1);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  launch_pdl(kv_finish_kernel, (c.B + 127) / 128, 128, 0, st, c.B, ts.N, c.K, c.L_cap, L, acc, path, kv_map);
-  note_launches(1);
   return cudaGetLastError();
 }
 

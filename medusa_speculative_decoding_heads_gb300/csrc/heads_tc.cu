@@ -12,7 +12,12 @@
 // columns of a sequence are added in the epilogue.
 //
 // Persistent CTAs (one per SM) walk a static list of work units (head, 128-row
-// tile, k-split); 6 warps:
+// tile, k range). The vocab projection takes whole tiles round robin. The
+// d x d residual layer has too few tiles for that to balance (e.g. 128 tiles
+// of 64 chunks on 152 SMs), so it splits the flat (tile, chunk) sequence into
+// equal contiguous ranges, one per CTA (a stream-K split): a range that
+// crosses tiles yields one unit per tile, each writing its partial sums to the
+// slot numbered by its position among the CTAs that share the tile. 6 warps:
 //   warp 4  TMA producer: 64-wide k chunks of the weight tile and of the vector
 //           tile into a deep shared-memory ring (128-byte swizzle).
 //   warp 5  MMA issuer: four K=16 MMAs per chunk into one of two TMEM
@@ -47,8 +52,44 @@ struct HeadsGeom {
   static constexpr int kSmem = kStages * kStage + 1024;
 };
 
-// out[ks][b][g][r] = sum_k A[g*rows + r][k] * X[g*x_rows + col(b)][k] over the
-// unit's k range; col(b) = b (+ NB for the lo part when HILO).
+// First CTA of a stream-K split whose chunk range reaches flat chunk x, for T
+// chunks over P CTAs (CTA c owns [c T / P, (c + 1) T / P)): the largest c with
+// floor(c T / P) <= x.
+__host__ __device__ __forceinline__ int stream_first_cta(long long x, long long T, long long P) {
+  return (int)(((x + 1) * P + T - 1) / T - 1);
+}
+
+// The i-th work unit of this CTA: head g, tile t, chunks [c0, c1), output slot.
+// Round robin: unit u = blockIdx.x + i * gridDim.x of G * tiles * ksplit, slot = k-split.
+// Stream: the i-th tile that this CTA's chunk range touches.
+template <bool kStream>
+__device__ __forceinline__ bool unit_of(int i, int G, int tiles, int nchunks, int nk, int ksplit, int& g, int& t,
+                                        int& c0, int& c1, int& slot) {
+  if (!kStream) {
+    const int u = blockIdx.x + i * gridDim.x;
+    if (u >= G * tiles * ksplit) return false;
+    slot = u % ksplit;
+    t = (u / ksplit) % tiles;
+    g = u / (ksplit * tiles);
+    c0 = slot * nk;
+    c1 = min(nchunks, c0 + nk);
+    return true;
+  }
+  const long long T = (long long)G * tiles * nchunks, P = gridDim.x;
+  const long long f0 = blockIdx.x * T / P, f1 = (blockIdx.x + 1) * T / P;
+  const long long tf = f0 / nchunks + i, s0 = tf * nchunks;
+  if (s0 >= f1) return false;
+  c0 = (int)((f0 > s0 ? f0 : s0) - s0);
+  c1 = (int)((f1 < s0 + nchunks ? f1 : s0 + nchunks) - s0);
+  g = (int)(tf / tiles);
+  t = (int)(tf % tiles);
+  slot = (int)blockIdx.x - stream_first_cta(s0, T, P);
+  return true;
+}
+
+// out[slot][b][g][r] = sum_k A[g*rows + r][k] * X[g*x_rows + col(b)][k] over the
+// unit's k range; col(b) = b (+ NB for the lo part when HILO). The residual
+// layer (!HILO) uses the stream-K schedule, the vocab projection round robin.
 template <int NCOL, bool HILO>
 __global__ void __launch_bounds__(192, 1)
 heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmX, int rows, int G,
@@ -66,8 +107,8 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   uint32_t* err = &g_heads_tc_error;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr bool kStream = !HILO;
   const int tiles = (rows + kRowsTile - 1) / kRowsTile;
-  const int nunits = G * tiles * ksplit;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -89,23 +130,18 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // Warm L2 with the weight boxes of this CTA's first S chunks while the
     // previous kernel finishes (a prefetch is only a hint, so it cannot observe
     // stale data; the real loads come after the wait below).
-    int n = 0;
-    for (int u = blockIdx.x; u < nunits && n < S; u += gridDim.x) {
-      const int ks = u % ksplit, t = (u / ksplit) % tiles, g = u / (ksplit * tiles);
-      const int c0 = ks * nk, c1 = min(nchunks, c0 + nk);
+    int n = 0, g, t, c0, c1, slot;
+    for (int i = 0; n < S && unit_of<kStream>(i, G, tiles, nchunks, nk, ksplit, g, t, c0, c1, slot); ++i)
       for (int c = c0; c < c1 && n < S; ++c, ++n) tc::tma_prefetch_2d(&tmA, c * kChunkK, g * rows + t * kRowsTile);
-    }
   }
   pdl_wait();   // the setup above overlaps the previous kernel's tail; no global access before this
 
   if (warp == 4) {
     if (lane == 0) {
       // ---------------------------------------------------------------- TMA producer
-      int it = 0;
+      int it = 0, g, t, c0, c1, slot;
       bool ok = true;
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-        const int ks = u % ksplit, t = (u / ksplit) % tiles, g = u / (ksplit * tiles);
-        const int c0 = ks * nk, c1 = min(nchunks, c0 + nk);
+      for (int i = 0; ok && unit_of<kStream>(i, G, tiles, nchunks, nk, ksplit, g, t, c0, c1, slot); ++i) {
         for (int c = c0; c < c1; ++c, ++it) {
           const int s = it % S;
           if (it >= S && !tc::mbar_wait(&empty[s], ((it / S) - 1) & 1, err, 1)) {
@@ -124,11 +160,9 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = tc::idesc_bf16_f32(kRowsTile, NCOL, 0, 0);
-      int it = 0, ui = 0;
+      int it = 0, ui = 0, g, t, c0, c1, slot;
       bool ok = true;
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++ui) {
-        const int ks = u % ksplit;
-        const int c0 = ks * nk, c1 = min(nchunks, c0 + nk);
+      for (; ok && unit_of<kStream>(ui, G, tiles, nchunks, nk, ksplit, g, t, c0, c1, slot); ++ui) {
         const int a = ui & 1;
         if (ui >= 2 && !tc::mbar_wait(&acc_empty[a], ((ui >> 1) - 1) & 1, err, 4)) break;
         tc::fence_after();
@@ -154,9 +188,8 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // ------------------------------------------------------------------ epilogue
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     const int i = threadIdx.x;
-    int ui = 0;
-    for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++ui) {
-      const int ks = u % ksplit, t = (u / ksplit) % tiles, g = u / (ksplit * tiles);
+    int g, t, c0, c1, slot;
+    for (int ui = 0; unit_of<kStream>(ui, G, tiles, nchunks, nk, ksplit, g, t, c0, c1, slot); ++ui) {
       const int a = ui & 1;
       const bool ok = tc::mbar_wait(&acc_full[a], (ui >> 1) & 1, err, 16);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -169,7 +202,7 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       tc::mbar_arrive(&acc_empty[a]);
       const int r = t * kRowsTile + i;
       if (r < rows) {
-        float* o = out + (size_t)ks * out_split_stride + (size_t)g * rows + r;
+        float* o = out + (size_t)slot * out_split_stride + (size_t)g * rows + r;
         const size_t bstride = (size_t)G * rows;
         constexpr int kCols = HILO ? NCOL / 2 : NCOL;   // batch columns (lo part follows when HILO)
 #pragma unroll
@@ -192,10 +225,13 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   }
 }
 
-// r = h + SiLU(sum_splits pre + bias); X2[k][n][o] = bf16(r), X2[k][NB+n][o] = bf16(r - bf16(r)).
-__global__ void residual_pack_tc_kernel(const float* __restrict__ part, int ksplit, const uint16_t* __restrict__ h,
-                                        const uint16_t* __restrict__ bias, uint16_t* __restrict__ X2, int B, int NB,
-                                        int K, int d) {
+// r = h + SiLU(sum_slots pre + bias); X2[k][n][o] = bf16(r), X2[k][NB+n][o] = bf16(r - bf16(r)).
+// Output o of head k lies in tile k * tiles + o / 128 of the residual layer's
+// stream-K split (nchunks chunks per tile over P CTAs); its partial sums sit
+// in the slots of the CTAs whose ranges touch that tile, added in slot order.
+__global__ void residual_pack_tc_kernel(const float* __restrict__ part, int tiles, int nchunks, int P,
+                                        const uint16_t* __restrict__ h, const uint16_t* __restrict__ bias,
+                                        uint16_t* __restrict__ X2, int B, int NB, int K, int d) {
   pdl_wait();
   pdl_trigger();
   // four consecutive outputs o per thread: 16-byte partial loads, 8-byte stores
@@ -210,7 +246,11 @@ __global__ void residual_pack_tc_kernel(const float* __restrict__ part, int kspl
     if (n < B) {
       float pre[4] = {0.f, 0.f, 0.f, 0.f};
       const float* pp = part + ((size_t)n * K + k) * d + o;
-      for (int s = 0; s < ksplit; ++s) {
+      // 32-bit form of stream_first_cta (the host checks that (T + 1) * P fits)
+      const uint32_t T = (uint32_t)(K * tiles * nchunks), tf = (uint32_t)(k * tiles + o / kRowsTile);
+      const uint32_t x0 = tf * nchunks, x1 = x0 + nchunks - 1;
+      const int nslots = (int)(((x1 + 1) * (uint32_t)P + T - 1) / T - ((x0 + 1) * (uint32_t)P + T - 1) / T) + 1;
+      for (int s = 0; s < nslots; ++s) {
         const float4 v = *reinterpret_cast<const float4*>(pp + s * split_stride);
         pre[0] += v.x;
         pre[1] += v.y;
@@ -244,13 +284,14 @@ template <int NCOL, bool HILO>
 cudaError_t run_gemv(const CUtensorMap& tmA, const CUtensorMap& tmX, int rows, int G, int x_rows, int nchunks, int ks,
                      int B, float* out, size_t out_split_stride, int num_sms, cudaStream_t st) {
   using Geo = HeadsGeom<NCOL>;
-  const int nk = (nchunks + ks - 1) / ks;   // ks comes from plan_heads_tc: every split has >= 1 chunk
+  const int nk = (nchunks + ks - 1) / ks;   // round robin: ks divides the chunks so that no split is empty
   const int tiles = (rows + kRowsTile - 1) / kRowsTile;
-  const int nunits = G * tiles * ks;
+  // stream-K (!HILO): one CTA per SM, or one per chunk when there are fewer chunks
+  const long long nunits = HILO ? (long long)G * tiles * ks : (long long)G * tiles * nchunks;
   cudaError_t e = cudaFuncSetAttribute(heads_tc_kernel<NCOL, HILO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Geo::kSmem);
   if (e != cudaSuccess) return e;
-  const int grid = nunits < num_sms ? nunits : num_sms;
+  const int grid = nunits < num_sms ? (int)nunits : num_sms;
   launch_pdl(heads_tc_kernel<NCOL, HILO>, grid, 192, Geo::kSmem, st, tmA, tmX, rows, G, x_rows, nchunks, nk, ks, B, out,
                                                               out_split_stride);
   note_launches(1);
@@ -262,12 +303,18 @@ int sm_count() {
   if (!n) {
     int dev = 0;
     cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
   }
   return n;
 }
 
 }  // namespace
+
+// CTAs of the residual layer's stream-K split.
+static int stream_ctas(const medusa_cfg& c) {
+  const long long T = (long long)c.K * ((c.d + kRowsTile - 1) / kRowsTile) * (c.d / kChunkK);
+  return (int)(T < sm_count() ? T : sm_count());
+}
 
 // Workspace layout of the tensor-core heads path.
 HeadsTcPlan plan_heads_tc(const medusa_cfg& c) {
@@ -275,12 +322,13 @@ HeadsTcPlan plan_heads_tc(const medusa_cfg& c) {
   p.NB = c.B <= 8 ? 8 : (c.B + 7) / 8 * 8;               // batch columns per part (hi or lo)
   p.NCOL1 = c.B <= 16 ? 16 : 32;                          // d x d layer: h only
   p.NCOL2 = 2 * p.NB;                                     // vocab projection: hi and lo
-  const int nchunks = c.d / kChunkK;
-  const int units1 = c.K * ((c.d + kRowsTile - 1) / kRowsTile);
-  int ks = (4 * 148 + units1 - 1) / units1;
-  ks = ks < 1 ? 1 : (ks > nchunks ? nchunks : ks);
-  const int nk = (nchunks + ks - 1) / ks;
-  p.ksplit1 = (nchunks + nk - 1) / nk;                    // no empty split
+  // partial-sum slots of the residual layer: at most the CTAs whose equal
+  // chunk ranges (>= floor(T / P) chunks each) can touch one tile
+  const long long nchunks = c.d / kChunkK;
+  const long long T = (long long)c.K * ((c.d + kRowsTile - 1) / kRowsTile) * nchunks;
+  const long long P = stream_ctas(c), per = T / P;
+  long long slots = (nchunks + per - 1) / per + 1;
+  p.slots1 = (int)(slots < P ? slots : P);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -288,7 +336,7 @@ HeadsTcPlan plan_heads_tc(const medusa_cfg& c) {
     return o;
   };
   p.x2 = take((size_t)c.K * p.NCOL2 * c.d * 2);
-  p.part1 = take((size_t)p.ksplit1 * c.B * c.K * c.d * 4);
+  p.part1 = take((size_t)p.slots1 * c.B * c.K * c.d * 4);
   p.total = off;
   return p;
 }
@@ -312,13 +360,16 @@ cudaError_t launch_heads_tc(const medusa_cfg& c, const void* h, const void* W, c
     return cudaErrorInvalidValue;
   const int sms = sm_count();
 
+  const int P1 = stream_ctas(c);
+  if (((long long)K * ((d + kRowsTile - 1) / kRowsTile) * nchunks + 1) * P1 >= (1LL << 32)) return cudaErrorInvalidValue;
   cudaError_t e = p.NCOL1 == 16
-                      ? run_gemv<16, false>(tmW, tmX1, d, K, 0, nchunks, p.ksplit1, B, part1, (size_t)B * K * d, sms, st)
-                      : run_gemv<32, false>(tmW, tmX1, d, K, 0, nchunks, p.ksplit1, B, part1, (size_t)B * K * d, sms, st);
+                      ? run_gemv<16, false>(tmW, tmX1, d, K, 0, nchunks, 1, B, part1, (size_t)B * K * d, P1, st)
+                      : run_gemv<32, false>(tmW, tmX1, d, K, 0, nchunks, 1, B, part1, (size_t)B * K * d, P1, st);
   if (e != cudaSuccess) return e;
   const int rp_blocks = (int)(((size_t)K * p.NB * (d / 4) + 255) / 256);
-  launch_pdl(residual_pack_tc_kernel, rp_blocks < 1024 ? rp_blocks : 1024, 256, 0, st, part1, p.ksplit1, static_cast<const uint16_t*>(h),
-                                               static_cast<const uint16_t*>(bias), x2, B, p.NB, K, d);
+  launch_pdl(residual_pack_tc_kernel, rp_blocks < 1024 ? rp_blocks : 1024, 256, 0, st, part1,
+             (d + kRowsTile - 1) / kRowsTile, nchunks, P1, static_cast<const uint16_t*>(h),
+             static_cast<const uint16_t*>(bias), x2, B, p.NB, K, d);
   note_launches(1);
   switch (p.NCOL2) {
     case 16: return run_gemv<16, true>(tmU, tmX2, V, K, p.NCOL2, nchunks, 1, B, z, 0, sms, st);

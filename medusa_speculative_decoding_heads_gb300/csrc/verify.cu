@@ -186,26 +186,42 @@ __device__ __forceinline__ void load8<float>(const float* row, int v, float* x) 
 // ---------------------------------------------------------------- row pass (parallel)
 constexpr int kRowThreads = 256;
 constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kMaxRowSlices = 8;   // CTAs per row in the greedy argmax pass
+constexpr int kMaxHsSlices = 8;    // CTAs per head row in the rejection-sampling stats pass
 
-// Greedy: amax[b][n] = argmax_v target[b][n][v] (lowest index on ties). grid (N, B).
-// VEC: rows are read 8 entries at a time (V % 8 == 0), all of a thread's loads in flight.
+// CTAs per row for a pass over `rows` rows of V entries: enough for about two
+// CTAs per SM, at most `cap`, each slice a multiple of 8 entries.
+int row_slices(long rows, int V, int cap) {
+  long p = (2 * 152 + rows - 1) / rows;
+  p = p < 1 ? 1 : (p > cap ? cap : p);
+  const long by_len = (V + 8 * kRowThreads - 1) / (8 * kRowThreads);   // at least 8 entries per thread
+  return (int)(p < by_len ? p : (by_len < 1 ? 1 : by_len));
+}
+int slice_len(int V, int P) { return ((V + P - 1) / P + 7) / 8 * 8; }
+
+// Greedy: the argmax of slice p of target row (b, n) (lowest index on ties),
+// part[(b * N + n) * P + p] = (value bits, index); grid (P, N, B). The walk
+// merges the P slices of the rows it visits with the same rule, which gives
+// the argmax of the whole row. VEC: slices start at multiples of 8 and are read
+// 8 entries at a time (V % 8 == 0), all of a thread's loads in flight.
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kRowThreads)
-row_argmax_kernel(const T* __restrict__ tl, int N, int V, int32_t* __restrict__ amax) {
+row_argmax_kernel(const T* __restrict__ tl, int N, int V, int chunk, int2* __restrict__ part) {
   pdl_wait();
   pdl_trigger();
-  const int n = blockIdx.x, b = blockIdx.y;
+  const int p = blockIdx.x, n = blockIdx.y, b = blockIdx.z, P = gridDim.x;
   const T* row = tl + ((size_t)b * N + n) * V;
+  const int v0 = min(V, p * chunk), v1 = min(V, v0 + chunk);
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   if (VEC) {
     constexpr int kU = 8;   // vectors per thread per round
-    for (int base = 0; base < V; base += kU * 8 * kRowThreads) {
+    for (int base = v0; base < v1; base += kU * 8 * kRowThreads) {
       float x[kU][8];
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int v = base + 8 * (threadIdx.x + u * kRowThreads);
-        if (v < V) load8<T>(row, v, x[u]);
+        if (v < v1) load8<T>(row, v, x[u]);
         else
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[u][e] = -INFINITY;
@@ -215,7 +231,7 @@ row_argmax_kernel(const T* __restrict__ tl, int N, int V, int32_t* __restrict__ 
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int v = base + 8 * (threadIdx.x + u * kRowThreads) + e;
-          if (better(x[u][e], v, bv, bi)) {
+          if (v < v1 && better(x[u][e], v, bv, bi)) {
             bv = x[u][e];
             bi = v;
           }
@@ -223,7 +239,7 @@ row_argmax_kernel(const T* __restrict__ tl, int N, int V, int32_t* __restrict__ 
     }
   } else {
 #pragma unroll 4
-    for (int v = threadIdx.x; v < V; v += kRowThreads) {
+    for (int v = v0 + threadIdx.x; v < v1; v += kRowThreads) {
       const float x = Elt<T>::load(row, v);
       if (better(x, v, bv, bi)) {
         bv = x;
@@ -259,7 +275,7 @@ row_argmax_kernel(const T* __restrict__ tl, int N, int V, int32_t* __restrict__ 
         bi = oi;
       }
     }
-    if (threadIdx.x == 0) amax[(size_t)b * N + n] = bi;
+    if (threadIdx.x == 0) part[((size_t)b * N + n) * P + p] = make_int2(__float_as_int(bv), bi);
   }
 }
 
@@ -279,47 +295,6 @@ __device__ __forceinline__ FF ff_add8(FF acc, const float* e) {
   return ff_add(ff_add(acc, a), b);
 }
 
-// Rejection sampling, head rows: m = max and Z = sum exp((v - m) / T) of every
-// head's logit row. grid (K, B); stats[b][k] = (m, Z). Two sweeps (the second
-// hits L2); rows with V % 8 == 0 are read 8 entries at a time.
-template <bool VEC>
-__global__ void __launch_bounds__(kRowThreads)
-head_stats_kernel(const float* __restrict__ hl, int K, int V, float c, float2* __restrict__ stats) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ Scratch<kRowWarps> s;
-  const int k = blockIdx.x, b = blockIdx.y;
-  const float* row = hl + ((size_t)b * K + k) * V;
-  float mx = -INFINITY;
-  if (VEC) {
-#pragma unroll 2
-    for (int v = 8 * threadIdx.x; v < V; v += 8 * kRowThreads) {
-      float x[8];
-      load8<float>(row, v, x);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx = fmaxf(mx, x[e]);
-    }
-  } else {
-    for (int v = threadIdx.x; v < V; v += kRowThreads) mx = fmaxf(mx, row[v]);
-  }
-  const float m = block_max(mx, s);
-  FF loc{0.f, 0.f};
-  if (VEC) {
-#pragma unroll 2
-    for (int v = 8 * threadIdx.x; v < V; v += 8 * kRowThreads) {
-      float x[8];
-      load8<float>(row, v, x);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = fast_exp2((x[e] - m) * c);
-      loc = ff_add8(loc, x);
-    }
-  } else {
-    for (int v = threadIdx.x; v < V; v += kRowThreads) loc = ff_add(loc, fast_exp2((row[v] - m) * c));
-  }
-  const FF z = block_sum_ff(loc, s);
-  if (threadIdx.x == 0) stats[(size_t)b * K + k] = make_float2(m, z.hi + z.lo);
-}
-
 // ---------------------------------------------------------------- walks
 struct WalkOut {
   int32_t* acc;
@@ -329,9 +304,23 @@ struct WalkOut {
   uint32_t* flags;
 };
 
+// The argmax of a whole target row from its P slice results.
+__device__ __forceinline__ int row_best(const int2* __restrict__ pr, int P) {
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int p = 0; p < P; ++p) {
+    const int2 q = pr[p];
+    if (better(__int_as_float(q.x), q.y, bv, bi)) {
+      bv = __int_as_float(q.x);
+      bi = q.y;
+    }
+  }
+  return bi;
+}
+
 // Greedy walk from the per-row argmax. One thread per sequence.
 __global__ void greedy_walk_kernel(TreeShape ts, int B, const int32_t* __restrict__ tokens,
-                                   const int32_t* __restrict__ first_child, const int32_t* __restrict__ amax,
+                                   const int32_t* __restrict__ first_child, const int2* __restrict__ part, int P,
                                    WalkOut w) {
   pdl_wait();
   pdl_trigger();
@@ -339,13 +328,12 @@ __global__ void greedy_walk_kernel(TreeShape ts, int B, const int32_t* __restric
   if (b >= B) return;
   const int N = ts.N, K = ts.K;
   const int32_t* tok = tokens + (size_t)b * N;
-  const int32_t* am = amax + (size_t)b * N;
   int32_t* path = w.path + (size_t)b * (K + 1);
   int32_t* out = w.out_tokens + (size_t)b * (K + 1);
   int cur = 0, acc = 0;
   path[0] = 0;
   for (int dep = 1; dep <= K; ++dep) {
-    const int a = am[cur];
+    const int a = row_best(part + ((size_t)b * N + cur) * P, P);
     const int fc = first_child[cur];
     int nx = -1;
     for (int j = 0; j < ts.s[dep] && fc >= 0 && fc + j < N; ++j)
@@ -356,7 +344,7 @@ __global__ void greedy_walk_kernel(TreeShape ts, int B, const int32_t* __restric
     ++acc;
     path[acc] = cur;
   }
-  out[acc] = am[cur];
+  out[acc] = row_best(part + ((size_t)b * N + cur) * P, P);
   for (int r = acc + 1; r <= K; ++r) {
     path[r] = -1;
     out[r] = -1;
@@ -521,6 +509,71 @@ __device__ MS block_ms(MS v, float c, Scratch<NW>& s) {
   }
   __syncthreads();
   return MS{s.bf, s.tot};
+}
+
+// Rejection sampling, head rows: (m, Z) of slice p of head row (b, k), with
+// m = max and Z = sum exp((v - m) / T) over the slice; part[(b * K + k) * P + p],
+// grid (P, K, B). Each thread reads 16 entries per round (all loads in flight)
+// and folds them into its running pair; the walk merges the P slices of a row
+// by rescaling to the larger max. VEC: slices start at multiples of 8 (V % 8 == 0).
+template <bool VEC>
+__global__ void __launch_bounds__(kRowThreads)
+head_stats_kernel(const float* __restrict__ hl, int K, int V, int chunk, float c, float2* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ Scratch<kRowWarps> s;
+  const int p = blockIdx.x, k = blockIdx.y, b = blockIdx.z, P = gridDim.x;
+  const float* row = hl + ((size_t)b * K + k) * V;
+  const int v0 = min(V, p * chunk), v1 = min(V, v0 + chunk);
+  constexpr int kPer = 16;
+  MS run{-INFINITY, FF{0.f, 0.f}};
+  for (int base = v0; base < v1; base += kPer * kRowThreads) {
+    float x[kPer];
+    if (VEC) {
+#pragma unroll
+      for (int i = 0; i < kPer / 8; ++i) {
+        const int v = base + 8 * (threadIdx.x + i * kRowThreads);
+        if (v < v1) load8<float>(row, v, x + 8 * i);
+        else
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[8 * i + e] = -INFINITY;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int v = base + threadIdx.x + i * kRowThreads;
+        x[i] = v < v1 ? row[v] : -INFINITY;
+      }
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) m = fmaxf(m, x[i]);
+    if (m == -INFINITY) continue;
+    FF sum{0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kPer; i += 8) {
+      float e8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) e8[e] = fast_exp2((x[i + e] - m) * c);
+      sum = ff_add8(sum, e8);
+    }
+    run = ms_merge(run, MS{m, sum}, c);
+  }
+  const MS blk = block_ms(run, c, s);
+  if (threadIdx.x == 0) part[((size_t)b * K + k) * P + p] = make_float2(blk.m, blk.s.hi + blk.s.lo);
+}
+
+// Merges the P slice pairs of one head row into (m, Z) of the whole row.
+// Unused slots hold (-inf, 0).
+__device__ __forceinline__ float2 merge_head_stats(const float2 (&hp)[kMaxHsSlices], float c) {
+  float M = -INFINITY;
+#pragma unroll
+  for (int p = 0; p < kMaxHsSlices; ++p) M = fmaxf(M, hp[p].x);
+  FF Z{0.f, 0.f};
+#pragma unroll
+  for (int p = 0; p < kMaxHsSlices; ++p)
+    if (hp[p].x != -INFINITY) Z = ff_add(Z, hp[p].y * fast_exp2((hp[p].x - M) * c));
+  return make_float2(M, Z.hi + Z.lo);
 }
 
 // Row max and softmax normaliser of a target row over this CTA's slice (all of
@@ -696,8 +749,8 @@ template <typename T, int C, bool VEC>
 __global__ void __launch_bounds__(kVThreads, 1)
 rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restrict__ tokens,
                const int32_t* __restrict__ first_child, const T* __restrict__ tl, const float* __restrict__ hl,
-               const float2* __restrict__ hstats, const float* __restrict__ u_acc, const float* __restrict__ u_res,
-               WalkOut w) {
+               const float2* __restrict__ hstats, int hsP, const float* __restrict__ u_acc,
+               const float* __restrict__ u_res, WalkOut w) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ float buf[];   // inverse-CDF transpose, [C][kPad]
@@ -737,7 +790,7 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
     // candidate j's logits and uniform: loads issued now, stored after the row sweep
     const bool fetch = dep <= K && threadIdx.x < ts.s[dep];
     float ct = 0.f, ch = 0.f, cu = 0.f;
-    float2 cq = make_float2(0.f, 0.f);
+    float2 hq[kMaxHsSlices];   // the slices of this depth's head-row (m, Z), merged after the sweep
     if (fetch) {
       const int fc = s_fc[cur];
       const int j = threadIdx.x;
@@ -745,7 +798,10 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
       ct = Elt<T>::load(trow, xt);
       ch = hl[((size_t)b * K + (dep - 1)) * V + xt];
       cu = u_acc[((size_t)b * K + (dep - 1)) * ts.s_max + j];
-      if (j == 0) cq = hstats[(size_t)b * K + dep - 1];
+      if (j == 0)
+#pragma unroll
+        for (int p = 0; p < kMaxHsSlices; ++p)
+          hq[p] = p < hsP ? hstats[((size_t)b * K + dep - 1) * hsP + p] : make_float2(-INFINITY, 0.f);
     }
     if (dep <= K) {
       // warm L2 with this CTA's slice of every child's target row (the next depth reads one of them)
@@ -770,7 +826,7 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
         int nc = 0;
         while (nc < ts.s[dep] && fc >= 0 && fc + nc < N) ++nc;
         cand_n = nc;
-        cand_q = cq;
+        cand_q = merge_head_stats(hq, c);
       }
     }
     if (dep == K + 1) {
@@ -861,7 +917,7 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
 
 template <typename T, int C, bool VEC>
 cudaError_t launch_rs_walk_v(const medusa_cfg& c, const TreeShape& ts, int ncta, int slice, const int32_t* tokens,
-                             const int32_t* first_child, const void* tl, const float* hl, const float2* stats,
+                             const int32_t* first_child, const void* tl, const float* hl, const float2* stats, int hsP,
                              const float* ua, const float* ur, const WalkOut& w, cudaStream_t st) {
   const size_t smem = (size_t)C * kPad * sizeof(float);
   auto kern = rs_walk_kernel<T, C, VEC>;
@@ -882,7 +938,7 @@ cudaError_t launch_rs_walk_v(const medusa_cfg& c, const TreeShape& ts, int ncta,
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, ts, c.V, slice, c.temperature, tokens, first_child, static_cast<const T*>(tl), hl,
-                         stats, ua, ur, w);
+                         stats, hsP, ua, ur, w);
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -891,11 +947,11 @@ cudaError_t launch_rs_walk_v(const medusa_cfg& c, const TreeShape& ts, int ncta,
 // Vector loads need V % 8 == 0 (aligned rows and slices) and at least 8 entries per thread.
 template <typename T, int C>
 cudaError_t launch_rs_walk(const medusa_cfg& c, const TreeShape& ts, int ncta, int slice, const int32_t* tokens,
-                           const int32_t* first_child, const void* tl, const float* hl, const float2* stats,
+                           const int32_t* first_child, const void* tl, const float* hl, const float2* stats, int hsP,
                            const float* ua, const float* ur, const WalkOut& w, cudaStream_t st) {
   if (C >= 8 && c.V % 8 == 0)
-    return launch_rs_walk_v<T, C, (C >= 8)>(c, ts, ncta, slice, tokens, first_child, tl, hl, stats, ua, ur, w, st);
-  return launch_rs_walk_v<T, C, false>(c, ts, ncta, slice, tokens, first_child, tl, hl, stats, ua, ur, w, st);
+    return launch_rs_walk_v<T, C, (C >= 8)>(c, ts, ncta, slice, tokens, first_child, tl, hl, stats, hsP, ua, ur, w, st);
+  return launch_rs_walk_v<T, C, false>(c, ts, ncta, slice, tokens, first_child, tl, hl, stats, hsP, ua, ur, w, st);
 }
 
 // CTAs per sequence: the largest power of two (at most 8) that keeps the whole
@@ -911,17 +967,19 @@ cudaError_t run_rs(const medusa_cfg& c, const TreeShape& ts, const int32_t* toke
                    const void* tl, const float* hl, const float* ua, const float* ur, const WalkOut& w, float2* stats,
                    cudaStream_t st) {
   const float cs = 1.4426950408889634f / c.temperature;
+  const int hsP = row_slices((long)c.B * ts.K, c.V, kMaxHsSlices);
+  const int hs_chunk = slice_len(c.V, hsP);
   if (c.V % 8 == 0)
-    launch_pdl(head_stats_kernel<true>, dim3(ts.K, c.B), kRowThreads, 0, st, hl, ts.K, c.V, cs, stats);
+    launch_pdl(head_stats_kernel<true>, dim3(hsP, ts.K, c.B), kRowThreads, 0, st, hl, ts.K, c.V, hs_chunk, cs, stats);
   else
-    launch_pdl(head_stats_kernel<false>, dim3(ts.K, c.B), kRowThreads, 0, st, hl, ts.K, c.V, cs, stats);
+    launch_pdl(head_stats_kernel<false>, dim3(hsP, ts.K, c.B), kRowThreads, 0, st, hl, ts.K, c.V, hs_chunk, cs, stats);
   note_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int ncta = rs_cluster_ctas(c.B);
   const int slice = (((c.V + ncta - 1) / ncta) + 7) / 8 * 8;
   const int need = (slice + kVThreads - 1) / kVThreads;
-#define MEDUSA_RS(CC) return launch_rs_walk<T, CC>(c, ts, ncta, slice, tokens, first_child, tl, hl, stats, ua, ur, w, st)
+#define MEDUSA_RS(CC) return launch_rs_walk<T, CC>(c, ts, ncta, slice, tokens, first_child, tl, hl, stats, hsP, ua, ur, w, st)
   if (need <= 1) MEDUSA_RS(1);
   if (need <= 2) MEDUSA_RS(2);
   if (need <= 4) MEDUSA_RS(4);
@@ -933,15 +991,19 @@ cudaError_t run_rs(const medusa_cfg& c, const TreeShape& ts, const int32_t* toke
 
 template <typename T>
 cudaError_t run_greedy(const medusa_cfg& c, const TreeShape& ts, const int32_t* tokens, const int32_t* first_child,
-                       const void* tl, const WalkOut& w, int32_t* amax, cudaStream_t st) {
+                       const void* tl, const WalkOut& w, int2* part, cudaStream_t st) {
+  const int P = row_slices((long)c.B * ts.N, c.V, kMaxRowSlices);
+  const int chunk = slice_len(c.V, P);
   if (c.V % 8 == 0)
-    launch_pdl(row_argmax_kernel<T, true>, dim3(ts.N, c.B), kRowThreads, 0, st, static_cast<const T*>(tl), ts.N, c.V, amax);
+    launch_pdl(row_argmax_kernel<T, true>, dim3(P, ts.N, c.B), kRowThreads, 0, st, static_cast<const T*>(tl), ts.N, c.V,
+               chunk, part);
   else
-    launch_pdl(row_argmax_kernel<T, false>, dim3(ts.N, c.B), kRowThreads, 0, st, static_cast<const T*>(tl), ts.N, c.V, amax);
+    launch_pdl(row_argmax_kernel<T, false>, dim3(P, ts.N, c.B), kRowThreads, 0, st, static_cast<const T*>(tl), ts.N, c.V,
+               chunk, part);
   note_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  launch_pdl(greedy_walk_kernel, (c.B + 127) / 128, 128, 0, st, ts, c.B, tokens, first_child, amax, w);
+  launch_pdl(greedy_walk_kernel, (c.B + 127) / 128, 128, 0, st, ts, c.B, tokens, first_child, part, P, w);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -950,8 +1012,8 @@ cudaError_t run_greedy(const medusa_cfg& c, const TreeShape& ts, const int32_t* 
 
 size_t verify_workspace(const medusa_cfg& c) {
   const TreeShape ts = tree_shape(c);
-  const size_t greedy = (size_t)c.B * ts.N * sizeof(int32_t);
-  const size_t rs = (size_t)c.B * ts.K * sizeof(float2);
+  const size_t greedy = (size_t)c.B * ts.N * kMaxRowSlices * sizeof(int2);
+  const size_t rs = (size_t)c.B * ts.K * kMaxHsSlices * sizeof(float2);
   return align_up(greedy > rs ? greedy : rs, 256);
 }
 
@@ -963,9 +1025,9 @@ cudaError_t launch_verify(const medusa_cfg& c, const int32_t* tokens, const int3
   const TreeShape ts = tree_shape(c);
   WalkOut w{acc, path, out_tokens, n_out, flags};
   if (c.mode == MEDUSA_GREEDY) {
-    int32_t* amax = static_cast<int32_t*>(ws);
-    return c.dtype == MEDUSA_F32 ? run_greedy<float>(c, ts, tokens, first_child, tl, w, amax, st)
-                                 : run_greedy<uint16_t>(c, ts, tokens, first_child, tl, w, amax, st);
+    int2* part = static_cast<int2*>(ws);
+    return c.dtype == MEDUSA_F32 ? run_greedy<float>(c, ts, tokens, first_child, tl, w, part, st)
+                                 : run_greedy<uint16_t>(c, ts, tokens, first_child, tl, w, part, st);
   }
   float2* stats = static_cast<float2*>(ws);
   return c.dtype == MEDUSA_F32 ? run_rs<float>(c, ts, tokens, first_child, tl, hl, u_acc, u_res, w, stats, st)

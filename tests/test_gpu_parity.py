@@ -125,6 +125,34 @@ def test_heads_full_size_sampled(name):
     check_heads(w, si, st, rows=pairs)
 
 
+@pytest.mark.parametrize("groups", [1, 7, 37, 997])
+@pytest.mark.parametrize("name", ["vicuna7b_b1", "vicuna13b_b8"])
+def test_heads_topk_ties(name, groups):
+    """Top-s under exact ties: vocabulary row v of every head copies row v % groups,
+    so each logit value repeats about V / groups times. The selection must be
+    the larger value first and the lower index among equal values, which a
+    stable sort of the library's own float32 logits defines. Few groups put
+    more tied entries at the threshold than the shortlist holds (the exact
+    per-thread path); many groups take the shortlist path."""
+    dev = gpu_ready()
+    w = configs.scaled(configs.get(name), d=128, V=5000, L_range=(40, 40), Hq=2, Hkv=2)
+    si = synth.make_step_inputs(w, seed=groups, device=dev)
+    U = si.U.clone()
+    src = torch.arange(w.V, device=dev) % groups
+    U[:] = U[:, src]
+    st = DeviceStep(w, w.modes[0], si.L_cap, dev)
+    st.heads(si.h, si.W, si.bias, U)
+    torch.cuda.synchronize()
+    z = st.logits.cpu().numpy()
+    topk = st.topk.cpu().numpy()
+    for b in range(w.B):
+        for k in range(w.K):
+            s = w.branching[k]
+            want = np.argsort(-z[b, k], kind="stable")[:s]
+            assert list(topk[b, k, :s]) == list(want), f"b={b} k={k}"
+            assert all(v == -1 for v in topk[b, k, s:])
+
+
 # --------------------------------------------------------------------------- attention
 def check_attention(w, si, O_gpu, pairs):
     tree = O.tree_layout(w.branching)
