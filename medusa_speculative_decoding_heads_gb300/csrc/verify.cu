@@ -398,7 +398,8 @@ __device__ __forceinline__ void cluster_sync() {
 }
 
 // All threads call with the same block-uniform value; returns every CTA's value in vals[rank].
-__device__ void xchg(Xchg& x, int& xn, float2 mine, float2* vals, uint32_t ncta, uint32_t rank, uint32_t* fl) {
+__device__ __forceinline__ void xchg(Xchg& x, int& xn, float2 mine, float2 (&vals)[kMaxCluster], uint32_t ncta,
+                                     uint32_t rank, uint32_t* fl) {
   const int par = xn & 1;
   __syncthreads();
   if (threadIdx.x < ncta) {
@@ -423,7 +424,8 @@ __device__ void xchg(Xchg& x, int& xn, float2 mine, float2* vals, uint32_t ncta,
       break;
     }
   }
-  for (uint32_t r = 0; r < ncta; ++r) vals[r] = x.f[par][r];
+#pragma unroll
+  for (uint32_t r = 0; r < kMaxCluster; ++r) vals[r] = r < ncta ? x.f[par][r] : make_float2(0.f, 0.f);
   ++xn;
 }
 
@@ -436,32 +438,13 @@ struct WalkState {
   int kept[kMaxS + 1];
 };
 
+// Unrolled over every possible level so that a register copy of the state is
+// indexed statically (a runtime-bounded loop would put it in local memory).
 __device__ __forceinline__ float apply_levels(const WalkState& ws, float p, float q) {
-  for (int j = 1; j <= ws.levels; ++j)
-    if (ws.kept[j]) p = fmaxf(0.f, p - q) * ws.inv_zr[j];
-  return p;
-}
-
-// One entry / 8 consecutive entries with the fast exponential (row sweeps); c = log2(e) / T.
-template <typename T>
-__device__ __forceinline__ float p_fast(const WalkState& ws, const T* trow, const float* hrow, float c, int v,
-                                        float* qv) {
-  const float q = hrow ? fast_exp2((hrow[v] - ws.mq) * c) * ws.inv_zq : 0.f;
-  *qv = q;
-  return apply_levels(ws, fast_exp2((Elt<T>::load(trow, v) - ws.mt) * c) * ws.inv_zt, q);
-}
-
-template <typename T>
-__device__ __forceinline__ void p_fast8(const WalkState& ws, const T* trow, const float* hrow, float c, int v0,
-                                        float* p, float* q) {
-  float t8[8], h8[8];
-  load8<T>(trow, v0, t8);
-  if (hrow) load8<float>(hrow, v0, h8);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    q[e] = hrow ? fast_exp2((h8[e] - ws.mq) * c) * ws.inv_zq : 0.f;
-    p[e] = apply_levels(ws, fast_exp2((t8[e] - ws.mt) * c) * ws.inv_zt, q[e]);
-  }
+  for (int j = 1; j <= kMaxS; ++j)
+    if (j <= ws.levels && ws.kept[j]) p = fmaxf(0.f, p - q) * ws.inv_zr[j];
+  return p;
 }
 
 // Entry v of this CTA's slice for thread t, step i: VEC takes 8 consecutive
@@ -576,29 +559,36 @@ __device__ __forceinline__ float2 merge_head_stats(const float2 (&hp)[kMaxHsSlic
   return make_float2(M, Z.hi + Z.lo);
 }
 
-// Row max and softmax normaliser of a target row over this CTA's slice (all of
-// a thread's entries are loaded first, so their latencies overlap), merged across
-// the block and then across the cluster by rescaling to the larger max.
+// This thread's C entries of a row slice [lo, hi), as floats, all loads in
+// flight at once; entries past hi read as `pad`. VEC: entry 8 i + e is
+// v = lo + 8 (t + i kVThreads) + e (V % 8 == 0, so a group of 8 is in or out
+// as a whole); otherwise entry i is v = lo + t + i kVThreads.
 template <typename T, int C, bool VEC>
-__device__ float2 target_stats(const T* trow, int lo, int hi, float c, Scratch<kVWarps>& s, Xchg& x, int& xn,
-                               uint32_t ncta, uint32_t rank, uint32_t* fl) {
-  float xv[C];
+__device__ __forceinline__ void load_slice(const T* row, int lo, int hi, float (&x)[C], float pad) {
   if (VEC) {
 #pragma unroll
     for (int i = 0; i < C / 8; ++i) {
       const int v0 = lo + 8 * (threadIdx.x + i * kVThreads);
-      if (v0 < hi) load8<T>(trow, v0, xv + 8 * i);
+      if (v0 < hi) load8<T>(row, v0, x + 8 * i);
       else
 #pragma unroll
-        for (int e = 0; e < 8; ++e) xv[8 * i + e] = -INFINITY;
+        for (int e = 0; e < 8; ++e) x[8 * i + e] = pad;
     }
   } else {
 #pragma unroll
     for (int i = 0; i < C; ++i) {
       const int v = lo + threadIdx.x + i * kVThreads;
-      xv[i] = v < hi ? Elt<T>::load(trow, v) : -INFINITY;
+      x[i] = v < hi ? Elt<T>::load(row, v) : pad;
     }
   }
+}
+
+// Row max and softmax normaliser of a target row from this thread's entries
+// xv (padded with -inf), merged across the block and then across the cluster
+// by rescaling to the larger max.
+template <int C>
+__device__ float2 target_stats(const float (&xv)[C], float c, Scratch<kVWarps>& s, Xchg& x, int& xn, uint32_t ncta,
+                               uint32_t rank, uint32_t* fl) {
   float mx = -INFINITY;
 #pragma unroll
   for (int i = 0; i < C; ++i) mx = fmaxf(mx, xv[i]);
@@ -616,77 +606,73 @@ __device__ float2 target_stats(const T* trow, int lo, int hi, float c, Scratch<k
   float2 vals[kMaxCluster];
   xchg(x, xn, make_float2(blk.m, blk.s.hi + blk.s.lo), vals, ncta, rank, fl);
   float M = -INFINITY;
-  for (uint32_t k = 0; k < ncta; ++k) M = fmaxf(M, vals[k].x);
+#pragma unroll
+  for (uint32_t k = 0; k < kMaxCluster; ++k)
+    if (k < ncta) M = fmaxf(M, vals[k].x);
   FF Z{0.f, 0.f};
-  for (uint32_t k = 0; k < ncta; ++k)
-    if (vals[k].x != -INFINITY) Z = ff_add(Z, vals[k].y * fast_exp2((vals[k].x - M) * c));
+#pragma unroll
+  for (uint32_t k = 0; k < kMaxCluster; ++k)
+    if (k < ncta && vals[k].x != -INFINITY) Z = ff_add(Z, vals[k].y * fast_exp2((vals[k].x - M) * c));
   return make_float2(M, Z.hi + Z.lo);
 }
 
-// Sum over the row of max(0, p_j - q) (the next residual's normaliser).
-template <typename T, int C, bool VEC>
-__device__ float residual_sum(const WalkState& ws, const T* trow, const float* hrow, float c, int lo, int hi,
-                              Scratch<kVWarps>& s, Xchg& x, int& xn, uint32_t ncta, uint32_t rank, uint32_t* fl) {
+// p_0 = softmax(target / T) and q = softmax(head / T) at this thread's entries
+// (c = log2(e) / T; padded entries give 0); without a head row q = 0.
+template <int C>
+__device__ __forceinline__ void start_levels(const float (&tv)[C], const float (&hv)[C], bool has_h,
+                                             const WalkState& ws, float c, float (&pc)[C], float (&qc)[C]) {
+#pragma unroll
+  for (int i = 0; i < C; ++i) {
+    pc[i] = fast_exp2((tv[i] - ws.mt) * c) * ws.inv_zt;
+    qc[i] = has_h ? fast_exp2((hv[i] - ws.mq) * c) * ws.inv_zq : 0.f;
+  }
+}
+
+// p_j -> p_{j+1} = max(0, p_j - q) / Z_{j+1} (skipped when Z_{j+1} < 1e-30), at
+// this thread's entries.
+template <int C>
+__device__ __forceinline__ void next_level(float (&pc)[C], const float (&qc)[C], float ft) {
+  if (!(ft >= 1e-30f)) return;
+  const float a = 1.f / ft;
+#pragma unroll
+  for (int i = 0; i < C; ++i) pc[i] = fmaxf(0.f, pc[i] - qc[i]) * a;
+}
+
+// Sum over the row of max(0, p_j - q) (the next residual's normaliser), from
+// this thread's p_j and q (zero past the slice).
+template <int C>
+__device__ float residual_sum(const float (&pc)[C], const float (&qc)[C], Scratch<kVWarps>& s, Xchg& x, int& xn,
+                              uint32_t ncta, uint32_t rank, uint32_t* fl) {
   FF loc{0.f, 0.f};
-  if (VEC) {
 #pragma unroll
-    for (int i = 0; i < C / 8; ++i) {
-      const int v0 = lo + 8 * (threadIdx.x + i * kVThreads);
-      if (v0 < hi) {
-        float p[8], q[8];
-        p_fast8<T>(ws, trow, hrow, c, v0, p, q);
+  for (int i = 0; i < C; i += 8) {
+    float d8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) p[e] = fmaxf(0.f, p[e] - q[e]);
-        loc = ff_add8(loc, p);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < C; ++i) {
-      const int v = lo + threadIdx.x + i * kVThreads;
-      if (v < hi) {
-        float q;
-        const float p = p_fast<T>(ws, trow, hrow, c, v, &q);
-        loc = ff_add(loc, fmaxf(0.f, p - q));
-      }
-    }
+    for (int e = 0; e < 8; ++e) d8[e] = (i + e < C) ? fmaxf(0.f, pc[i + e] - qc[i + e]) : 0.f;
+    loc = ff_add8(loc, d8);
   }
   const FF tot = block_sum_ff(loc, s);
   float2 vals[kMaxCluster];
   xchg(x, xn, make_float2(tot.hi, tot.lo), vals, ncta, rank, fl);
   FF all{0.f, 0.f};
-  for (uint32_t k = 0; k < ncta; ++k) all = ff_add(all, FF{vals[k].x, vals[k].y});
+#pragma unroll
+  for (uint32_t k = 0; k < kMaxCluster; ++k)
+    if (k < ncta) all = ff_add(all, FF{vals[k].x, vals[k].y});
   return all.hi + all.lo;
 }
 
-// Inverse CDF of the current p over the row (smallest y with cdf(y) > u * total);
-// sets *near for the 1e-6 tie band.
-template <typename T, int C, bool VEC>
-__device__ int walk_inverse_cdf(const WalkState& ws, const T* trow, const float* hrow, float c, int lo, int hi,
-                                int V, float u, float* buf, Scratch<kVWarps>& s, Xchg& x, int& xn, uint32_t ncta,
-                                uint32_t rank, uint32_t* fl, bool* near) {
+// Inverse CDF of the current p over the row (smallest y with cdf(y) > u * total),
+// from this thread's p (zero past the slice); sets *near for the 1e-6 tie band.
+template <int C, bool VEC>
+__device__ int walk_inverse_cdf(const float (&pc)[C], int lo, int hi, int V, float u, float* buf,
+                                Scratch<kVWarps>& s, Xchg& x, int& xn, uint32_t ncta, uint32_t rank, uint32_t* fl,
+                                bool* near) {
   __syncthreads();
-  // this CTA's slice, local index lv = v - lo, into the transpose
-  if (VEC) {
+  // this thread's entries, local index l = v - lo, into the transpose
 #pragma unroll
-    for (int i = 0; i < C / 8; ++i) {
-      const int l0 = 8 * (threadIdx.x + i * kVThreads);
-      float p[8], q[8];
-      if (lo + l0 < hi) p_fast8<T>(ws, trow, hrow, c, lo + l0, p, q);
-      else
-#pragma unroll
-        for (int e = 0; e < 8; ++e) p[e] = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) buf[((l0 + e) % C) * kPad + (l0 + e) / C] = p[e];
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < C; ++i) {
-      const int l = threadIdx.x + i * kVThreads;
-      float q;
-      const float p = lo + l < hi ? p_fast<T>(ws, trow, hrow, c, lo + l, &q) : 0.f;
-      buf[(l % C) * kPad + l / C] = p;
-    }
+  for (int i = 0; i < C; ++i) {
+    const int l = VEC ? 8 * (threadIdx.x + (i / 8) * kVThreads) + (i % 8) : threadIdx.x + i * kVThreads;
+    buf[(l % C) * kPad + l / C] = pc[i];
   }
   __syncthreads();
   const int l0 = threadIdx.x * C;   // this thread now holds local entries [l0, l0 + C)
@@ -699,10 +685,12 @@ __device__ int walk_inverse_cdf(const WalkState& ws, const T* trow, const float*
   float2 vals[kMaxCluster];
   xchg(x, xn, make_float2(cta_total.hi, cta_total.lo), vals, ncta, rank, fl);
   FF total{0.f, 0.f}, before{0.f, 0.f};
-  for (uint32_t k = 0; k < ncta; ++k) {
-    if (k == rank) before = total;
-    total = ff_add(total, FF{vals[k].x, vals[k].y});
-  }
+#pragma unroll
+  for (uint32_t k = 0; k < kMaxCluster; ++k)
+    if (k < ncta) {
+      if (k == rank) before = total;
+      total = ff_add(total, FF{vals[k].x, vals[k].y});
+    }
   cum = ff_add(before, cum);
   const float th = u * total.hi;
   const FF thr = ff_norm(th, fmaf(u, total.hi, -th) + u * total.lo);   // u * total as an exact pair
@@ -728,13 +716,15 @@ __device__ int walk_inverse_cdf(const WalkState& ws, const T* trow, const float*
   // the first slice holding a crossing wins
   xchg(x, xn, make_float2(__int_as_float(y_cta), __int_as_float(near_flag)), vals, ncta, rank, fl);
   int y = 0x7fffffff, nf = 0;
-  for (uint32_t k = 0; k < ncta; ++k) {
-    const int yk = __float_as_int(vals[k].x);
-    if (yk < y) {
-      y = yk;
-      nf = __float_as_int(vals[k].y);
+#pragma unroll
+  for (uint32_t k = 0; k < kMaxCluster; ++k)
+    if (k < ncta) {
+      const int yk = __float_as_int(vals[k].x);
+      if (yk < y) {
+        y = yk;
+        nf = __float_as_int(vals[k].y);
+      }
     }
-  }
   *near = nf != 0;
   if (y == 0x7fffffff) {   // only reachable if rounding left u*total at or above the last cumulative sum
     *near = true;
@@ -815,7 +805,15 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
         }
       }
     }
-    const float2 tst = target_stats<T, C, VEC>(trow, lo, hi, c, s, x, xn, ncta, rank, &fl);
+    // this thread's entries of the node's target row and of the depth's head row
+    float tv[C], hv[C];
+    load_slice<T, C, VEC>(trow, lo, hi, tv, -INFINITY);
+    if (dep <= K) load_slice<float, C, VEC>(hl + ((size_t)b * K + (dep - 1)) * V, lo, hi, hv, -INFINITY);
+    else
+#pragma unroll
+      for (int i = 0; i < C; ++i) hv[i] = -INFINITY;
+    const float2 tst = target_stats<C>(tv, c, s, x, xn, ncta, rank, &fl);
+    float pc[C], qc[C];   // p_j and q at this thread's entries
     if (fetch) {
       const int fc = s_fc[cur];
       const int j = threadIdx.x;
@@ -838,14 +836,14 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
         ws.levels = 0;
       }
       __syncthreads();
+      start_levels<C>(tv, hv, false, ws, c, pc, qc);
       bool near = false;
-      const int y = walk_inverse_cdf<T, C, VEC>(ws, trow, nullptr, c, lo, hi, V, u_res[(size_t)b * (K + 1) + K], buf,
-                                                s, x, xn, ncta, rank, &fl, &near);
+      const int y = walk_inverse_cdf<C, VEC>(pc, lo, hi, V, u_res[(size_t)b * (K + 1) + K], buf, s, x, xn, ncta, rank,
+                                             &fl, &near);
       if (near) fl |= MEDUSA_FLAG_CDF_NEAR_TIE;
       if (threadIdx.x == 0) out[acc] = y;
       break;
     }
-    const float* hrow = hl + ((size_t)b * K + (dep - 1)) * V;
     __syncthreads();
     if (threadIdx.x == 0) {
       const float2 q = cand_q;
@@ -856,6 +854,7 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
       ws.levels = 0;
     }
     __syncthreads();
+    start_levels<C>(tv, hv, true, ws, c, pc, qc);
     const int fc = s_fc[cur];
     const int nc = cand_n;
     int accepted = -1;
@@ -871,7 +870,8 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
         break;
       }
       // residual: Z_{j+1} = sum_v max(0, p_j(v) - q(v)) over the row
-      const float ft = residual_sum<T, C, VEC>(ws, trow, hrow, c, lo, hi, s, x, xn, ncta, rank, &fl);
+      const float ft = residual_sum<C>(pc, qc, s, x, xn, ncta, rank, &fl);
+      next_level<C>(pc, qc, ft);
       __syncthreads();
       if (threadIdx.x == 0) {
         const int l = ws.levels + 1;
@@ -883,8 +883,8 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
     }
     if (accepted < 0) {
       bool near = false;
-      const int y = walk_inverse_cdf<T, C, VEC>(ws, trow, hrow, c, lo, hi, V, u_res[(size_t)b * (K + 1) + (dep - 1)],
-                                                buf, s, x, xn, ncta, rank, &fl, &near);
+      const int y = walk_inverse_cdf<C, VEC>(pc, lo, hi, V, u_res[(size_t)b * (K + 1) + (dep - 1)], buf, s, x, xn,
+                                             ncta, rank, &fl, &near);
       if (near) fl |= MEDUSA_FLAG_CDF_NEAR_TIE;
       if (threadIdx.x == 0) out[acc] = y;
       break;
