@@ -255,6 +255,33 @@ def test_verify_greedy_bit_exact(name):
     assert len(set(ref["acc"].tolist())) > 1
 
 
+@pytest.mark.parametrize("name", ["vicuna7b_b1", "vicuna33b_b16"])
+def test_repeated_calls_share_workspace(name):
+    """A workspace carries nothing from one call into the next: the same heads
+    and greedy-verify calls, issued three times on one workspace (the last time
+    after a heads call on other inputs), give identical results."""
+    dev = gpu_ready()
+    w = configs.scaled(configs.get(name), d=256, V=3000, L_range=(40, 40), Hq=2, Hkv=2, target_corr=0.0)
+    si = synth.make_step_inputs(w, seed=3, device=dev)
+    L, L_cap, root, topk, tree, tl, depths = greedy_case(w, dev, seed=9)
+    st = st2 = DeviceStep(w, GREEDY, L_cap, dev)
+    outs = []
+    for rep in range(3):
+        if rep == 2:   # other inputs through the same workspace first
+            st.heads(si.h * 0.5, si.W, si.bias, si.U)
+        st.heads(si.h, si.W, si.bias, si.U)
+        st2.tree_build(torch.from_numpy(root).to(dev), torch.from_numpy(L).to(dev),
+                       topk=torch.from_numpy(topk).to(dev))
+        st2.verify(tl)
+        torch.cuda.synchronize()
+        outs.append((st.topk.cpu().numpy().copy(), i64(st2.acc).copy(), i64(st2.out_tokens).copy()))
+    for o in outs[1:]:
+        for a, b in zip(outs[0], o):
+            assert np.array_equal(a, b)
+    ref = O.verify_batch(GREEDY, tree, f64(tl), w.K)
+    assert np.array_equal(outs[-1][1], ref["acc"]) and np.array_equal(outs[-1][2], ref["out_tokens"])
+
+
 def rs_case(w, dev, seed, sigma_head=2.0):
     """Stand-in head logits (float32) and correlated target logits, identical for both sides."""
     gen = torch.Generator(device=dev)
