@@ -441,67 +441,46 @@ __device__ __forceinline__ void warp_top_s_t(float* lv, int* li, float* ov, int*
   }
 }
 
-// Shared memory of one top-s CTA (declared once per kernel, not per S).
-struct TopkSmem {
-  static constexpr int kCand = 128;
-  float wv[kTopThreads / 32][kMaxS];
-  int wi[kTopThreads / 32][kMaxS];
-  float cand_v[kCand];
-  int cand_i[kCand];
-  float wmax[kTopThreads / 32];
-  int cand_n;
-};
-
-// Calls f(x, v) for every entry v of row[v0, v1) that this thread owns: warp
-// w takes the w-th of eight contiguous parts of the slice and its lanes stride
-// through it, so every warp sees data once the slice has 8 (VEC4: 32) entries.
-// With VEC4 (rows and slices aligned to 4 floats) the entries arrive as
-// 16-byte loads, four of them in flight per thread.
-template <bool VEC4, class F>
-__device__ __forceinline__ void slice_for_each(const float* __restrict__ row, int v0, int v1, F&& f) {
-  constexpr int kW = kTopThreads / 32;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// One CTA: the S best of row[v0, v1). With VEC4 (rows and slices aligned to 4
+// floats) every thread issues two 16-byte loads per step before inserting.
+template <int S, bool VEC4>
+__device__ __forceinline__ void topk_slice(const float* __restrict__ row, int v0, int v1, float* __restrict__ out_v,
+                                           int* __restrict__ out_i) {
+  float lv[S];
+  int li[S];
+#pragma unroll
+  for (int i = 0; i < S; ++i) {
+    lv[i] = -INFINITY;
+    li[i] = 0x7fffffff;
+  }
   if (VEC4) {
     const float4* r4 = reinterpret_cast<const float4*>(row);
-    const int n4 = (v1 - v0) >> 2;
-    const int e1 = (v0 >> 2) + (warp + 1) * n4 / kW;
-    int g = (v0 >> 2) + warp * n4 / kW + lane;
-    for (; g + 96 < e1; g += 128) {
-      float4 a[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) a[u] = r4[g + 32 * u];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int v = 4 * (g + 32 * u);
-        f(a[u].x, v);
-        f(a[u].y, v + 1);
-        f(a[u].z, v + 2);
-        f(a[u].w, v + 3);
+    const int g0 = v0 >> 2, g1 = v1 >> 2;
+    for (int g = g0 + threadIdx.x; g < g1; g += 2 * kTopThreads) {
+      const float4 a = r4[g];
+      const bool two = g + kTopThreads < g1;
+      const float4 c = two ? r4[g + kTopThreads] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      list_insert_s<S>(lv, li, a.x, 4 * g);
+      list_insert_s<S>(lv, li, a.y, 4 * g + 1);
+      list_insert_s<S>(lv, li, a.z, 4 * g + 2);
+      list_insert_s<S>(lv, li, a.w, 4 * g + 3);
+      if (two) {
+        const int gc = g + kTopThreads;
+        list_insert_s<S>(lv, li, c.x, 4 * gc);
+        list_insert_s<S>(lv, li, c.y, 4 * gc + 1);
+        list_insert_s<S>(lv, li, c.z, 4 * gc + 2);
+        list_insert_s<S>(lv, li, c.w, 4 * gc + 3);
       }
     }
-    for (; g < e1; g += 32) {
-      const float4 a = r4[g];
-      f(a.x, 4 * g);
-      f(a.y, 4 * g + 1);
-      f(a.z, 4 * g + 2);
-      f(a.w, 4 * g + 3);
-    }
   } else {
-    const int n = v1 - v0;
-    const int e1 = v0 + (warp + 1) * n / kW;
-    for (int v = v0 + warp * n / kW + lane; v < e1; v += 32) f(row[v], v);
+    for (int v = v0 + threadIdx.x; v < v1; v += kTopThreads) list_insert_s<S>(lv, li, row[v], v);
   }
-}
-
-// Block-wide S best of every thread's sorted list (lists of length S in
-// registers); the result is valid in lane 0 of warp 0.
-template <int S>
-__device__ __forceinline__ void block_top_s(float* lv, int* li, float* tv, int* ti, TopkSmem& sm) {
-  auto& wv = sm.wv;
-  auto& wi = sm.wi;
+  __shared__ float wv[kTopThreads / 32][kMaxS];
+  __shared__ int wi[kTopThreads / 32][kMaxS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float tv[S];
+  int ti[S];
   warp_top_s_t<S>(lv, li, tv, ti);
-  __syncthreads();   // a previous use of wv / wi is complete
   if (lane == 0)
 #pragma unroll
     for (int r = 0; r < S; ++r) {
@@ -518,86 +497,13 @@ __device__ __forceinline__ void block_top_s(float* lv, int* li, float* tv, int* 
       li[i] = have ? wi[lane][i] : 0x7fffffff;
     }
     warp_top_s_t<S>(lv, li, tv, ti);
-  }
-}
-
-// One CTA: the S best of row[v0, v1) (larger value first, lower index on ties).
-// Two passes: the eight warps' maxima give a threshold t, the S-th largest of
-// them (S <= 8); those S maxima are S distinct entries >= t, so no entry below
-// t can be among the S best, and the second pass collects only the entries
-// >= t (typically a handful) into shared memory, where each one's rank among
-// them is counted directly. If more than kCand entries reach t (heavy ties at
-// the threshold), every thread keeps an exact sorted list of its entries instead.
-template <int S, bool VEC4>
-__device__ __forceinline__ void topk_slice(const float* __restrict__ row, int v0, int v1, float* __restrict__ out_v,
-                                           int* __restrict__ out_i, TopkSmem& sm) {
-  static_assert(S <= kTopThreads / 32, "the threshold needs S warp maxima");
-  constexpr int kCand = TopkSmem::kCand;
-  constexpr int kW = kTopThreads / 32;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float mx = -INFINITY;
-  slice_for_each<VEC4>(row, v0, v1, [&](float x, int) { mx = fmaxf(mx, x); });
+    if (lane == 0)
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) sm.wmax[warp] = mx;
-  if (threadIdx.x == 0) sm.cand_n = 0;
-  __syncthreads();
-  // t = the S-th largest warp maximum (ties broken by warp index)
-  float t = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < kW; ++i) {
-    const float wi = sm.wmax[i];
-    int rank = 0;
-#pragma unroll
-    for (int j = 0; j < kW; ++j) {
-      const float wj = sm.wmax[j];
-      rank += (wj > wi || (wj == wi && j < i)) ? 1 : 0;
-    }
-    if (rank == S - 1) t = wi;
-  }
-  slice_for_each<VEC4>(row, v0, v1, [&](float x, int v) {
-    if (x >= t) {
-      const int k = atomicAdd(&sm.cand_n, 1);
-      if (k < kCand) {
-        sm.cand_v[k] = x;
-        sm.cand_i[k] = v;
+      for (int r = 0; r < S; ++r) {
+        out_v[r] = tv[r];
+        out_i[r] = ti[r];
       }
-    }
-  });
-  __syncthreads();
-  const int n = sm.cand_n;
-  if (n <= kCand) {
-    for (int k = threadIdx.x; k < n; k += kTopThreads) {
-      const float x = sm.cand_v[k];
-      const int v = sm.cand_i[k];
-      int rank = 0;
-      for (int j = 0; j < n; ++j) rank += better(sm.cand_v[j], sm.cand_i[j], x, v) ? 1 : 0;
-      if (rank < S) {
-        out_v[rank] = x;
-        out_i[rank] = v;
-      }
-    }
-    for (int r = n + threadIdx.x; r < S; r += kTopThreads) {   // fewer than S entries in the slice
-      out_v[r] = -INFINITY;
-      out_i[r] = 0x7fffffff;
-    }
-    return;
   }
-  float lv[S], tv[S];
-  int li[S], ti[S];
-#pragma unroll
-  for (int i = 0; i < S; ++i) {
-    lv[i] = -INFINITY;
-    li[i] = 0x7fffffff;
-  }
-  slice_for_each<VEC4>(row, v0, v1, [&](float x, int v) { list_insert_s<S>(lv, li, x, v); });
-  block_top_s<S>(lv, li, tv, ti, sm);
-  if (threadIdx.x == 0)
-#pragma unroll
-    for (int r = 0; r < S; ++r) {
-      out_v[r] = tv[r];
-      out_i[r] = ti[r];
-    }
 }
 
 // grid (P, K, B): slice p of row (b, k) -> s candidates at cand[((b*K + k)*P + p)*s_max + r].
@@ -612,16 +518,15 @@ topk_partial_kernel(const float* __restrict__ z, int V, TreeShape ts, int chunk,
   const float* row = z + ((size_t)b * K + k) * V;
   const int v0 = min(V, p * chunk), v1 = min(V, v0 + chunk);
   const size_t o = (((size_t)b * K + k) * P + p) * s_max;
-  __shared__ TopkSmem sm;
   switch (s) {
-    case 1: topk_slice<1, VEC4>(row, v0, v1, cv + o, ci + o, sm); break;
-    case 2: topk_slice<2, VEC4>(row, v0, v1, cv + o, ci + o, sm); break;
-    case 3: topk_slice<3, VEC4>(row, v0, v1, cv + o, ci + o, sm); break;
-    case 4: topk_slice<4, VEC4>(row, v0, v1, cv + o, ci + o, sm); break;
-    case 5: topk_slice<5, VEC4>(row, v0, v1, cv + o, ci + o, sm); break;
-    case 6: topk_slice<6, VEC4>(row, v0, v1, cv + o, ci + o, sm); break;
-    case 7: topk_slice<7, VEC4>(row, v0, v1, cv + o, ci + o, sm); break;
-    default: topk_slice<8, VEC4>(row, v0, v1, cv + o, ci + o, sm); break;
+    case 1: topk_slice<1, VEC4>(row, v0, v1, cv + o, ci + o); break;
+    case 2: topk_slice<2, VEC4>(row, v0, v1, cv + o, ci + o); break;
+    case 3: topk_slice<3, VEC4>(row, v0, v1, cv + o, ci + o); break;
+    case 4: topk_slice<4, VEC4>(row, v0, v1, cv + o, ci + o); break;
+    case 5: topk_slice<5, VEC4>(row, v0, v1, cv + o, ci + o); break;
+    case 6: topk_slice<6, VEC4>(row, v0, v1, cv + o, ci + o); break;
+    case 7: topk_slice<7, VEC4>(row, v0, v1, cv + o, ci + o); break;
+    default: topk_slice<8, VEC4>(row, v0, v1, cv + o, ci + o); break;
   }
 }
 
