@@ -156,12 +156,14 @@ MEDUSA_API int medusa_tree_attention(const medusa_cfg* cfg, const void* Q, const
  *   (-1 pad); n_out [B] = acc + 1; flags [B] uint32: this call ORs in its
  *   MEDUSA_FLAG_* bits (clear or initialise it first, e.g. with medusa_tree_build);
  *   MEDUSA_FLAG_TIMEOUT marks a sequence whose walk gave up on a bounded wait.
- * GREEDY reduces every tree node's target row to its argmax in parallel first,
- * so the walk itself is a few table lookups. REJECTION reduces every head row
- * (max and softmax normaliser) in parallel first; each sequence's walk then runs
- * on a cluster of up to 8 CTAs that split the vocabulary, trading their partial
- * sums through distributed shared memory: one sweep of the visited target row
- * per depth, one more per rejection and one for the final draw.
+ * GREEDY reduces every tree node's target row to its argmax in parallel first
+ * (rows split over several CTAs), so the walk itself is a few table lookups.
+ * REJECTION reduces every head row (max and softmax normaliser) in parallel
+ * first; each sequence's walk then runs on a cluster of up to 8 CTAs that split
+ * the vocabulary and trade their partial sums through distributed shared
+ * memory: per depth one load of the visited target row and the depth's head
+ * row (kept in registers), then one exchange per statistic, per rejection and
+ * for the final draw.
  * GREEDY: the child whose token equals argmax(target_logits[node]) (ties to
  * the lowest id) is accepted until none matches; the bonus is that argmax at
  * the last accepted node.
