@@ -199,6 +199,19 @@ def cpu_cores():
 
 
 # ----------------------------------------------------------------------------- reference arm
+def workload_config(w, L, mode, world):
+    """The `config` object of both arms' JSON lines: the workload, its sizes and lengths."""
+    elt = 4 if w.dtype == F32 else 2
+    weights = w.K * (w.d * w.d + w.d * w.V) * elt
+    kv = int(np.sum(L)) * w.Hkv * w.D * 2 * elt
+    return {"workload": w.name, "B": w.B, "d": w.d, "V": w.V, "K": w.K, "branching": list(w.branching),
+            "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "L": [int(x) for x in L][:4],
+            "L_sum": int(np.sum(L)), "mode": "greedy" if mode == GREEDY else "rejection",
+            "temperature": w.temperature if mode == REJECTION else None,
+            "l2": f"inputs larger than L2 ({(weights + kv) / 1e9:.2f} GB of weights and KV per step)",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -209,6 +222,7 @@ def run_reference(args):
     si = synth.make_step_inputs(w, seed=args.seed, device=dev)
     tl = make_targets(w, si, dev, mode, args.seed, via_library=False)
     x = oracle_inputs_from(si, tl)
+    L = np.asarray(si.L)
     del si, tl
     if dev == "cuda":
         torch.cuda.empty_cache()
@@ -218,7 +232,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": len(times), "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": w.name, "B": w.B, "mode": "greedy" if mode == GREEDY else "rejection"},
+            "data": "synthetic", "config": workload_config(w, L, mode, args.gpus),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                              "sample": f"one full oracle step of {w.name} (B={w.B}) per timed step"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -412,12 +426,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32" if w.dtype == F32 else "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "d": w.d, "V": w.V, "K": w.K, "branching": list(w.branching),
-                   "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "L": [int(x) for x in si.L][:4],
-                   "L_sum": int(np.sum(si.L)), "mode": "greedy" if mode == GREEDY else "rejection",
-                   "temperature": w.temperature if mode == REJECTION else None,
-                   "l2": f"inputs larger than L2 ({by['total'] / 1e9:.2f} GB algorithmic per step)",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(w, si.L, mode, world),
         "clocks": dict(clocks or {}, window=f"{args.soak:.1f} s soak of the same step + the timed region"),
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "kernel": "medusa_heads (residual + vocab projection GEMV, top-s)",
