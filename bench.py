@@ -40,7 +40,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per medusa_heads call, from the committed ncu capture of the heads
 # kernels on a reduced vocabulary (V=8000: traffic 1.02x the algorithmic
 # weight bytes), scaled to the workload's weight rows. Absent = not captured.
-NCU_TRAFFIC_BYTES = {"vicuna7b_b1": 1189563648}   # dram read + write of the medusa_heads kernels, one call
+NCU_TRAFFIC_BYTES = {"vicuna7b_b1": 1189563648, "vicuna7b_b1_shared": 402850048}   # dram read + write of the medusa_heads kernels, one call
 
 
 def parse():
@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=configs.ORDER)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=configs.ORDER + configs.SHARED)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -126,7 +126,8 @@ def algorithmic_bytes(w, L, acc, mode, with_bias=False):
     """Minimum bytes one step must move (each term counted once)."""
     elt = w.elt
     B, d, V, K, N = w.B, w.d, w.V, w.K, w.N
-    heads = K * (d * d + d * V + (d if with_bias else 0)) * elt + B * d * elt
+    vocab = (1 if w.shared_vocab else K) * d * V   # one shared projection is streamed once for all heads
+    heads = (K * (d * d + (d if with_bias else 0)) + vocab) * elt + B * d * elt
     logits = 2 * B * K * V * 4 if mode == REJECTION else 0
     kv = int(np.sum(L)) * w.Hkv * w.D * 2 * elt
     tree = B * N * (w.Hq + 2 * w.Hkv) * w.D * elt
@@ -202,12 +203,12 @@ def cpu_cores():
 def workload_config(w, L, mode, world):
     """The `config` object of both arms' JSON lines: the workload, its sizes and lengths."""
     elt = 4 if w.dtype == F32 else 2
-    weights = w.K * (w.d * w.d + w.d * w.V) * elt
+    weights = (w.K * w.d * w.d + (1 if w.shared_vocab else w.K) * w.d * w.V) * elt
     kv = int(np.sum(L)) * w.Hkv * w.D * 2 * elt
     return {"workload": w.name, "B": w.B, "d": w.d, "V": w.V, "K": w.K, "branching": list(w.branching),
             "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "L": [int(x) for x in L][:4],
             "L_sum": int(np.sum(L)), "mode": "greedy" if mode == GREEDY else "rejection",
-            "temperature": w.temperature if mode == REJECTION else None,
+            "temperature": w.temperature if mode == REJECTION else None, "shared_vocab": w.shared_vocab,
             "l2": f"inputs larger than L2 ({(weights + kv) / 1e9:.2f} GB of weights and KV per step)",
             "parallelism": f"replicas x{world}"}
 

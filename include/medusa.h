@@ -88,6 +88,11 @@ typedef struct {
   int32_t dtype;        /* MEDUSA_F32 or MEDUSA_BF16                             */
   int32_t mode;         /* MEDUSA_GREEDY or MEDUSA_REJECTION                     */
   float temperature;    /* T > 0 for MEDUSA_REJECTION (logits are divided by T)  */
+  int32_t shared_vocab; /* 0: one vocab projection U_k per head; 1: all heads    */
+                        /* share one frozen projection U (the base model's LM    */
+                        /* head), "Medusa 심층 아키텍처", section "잔차 블록을     */
+                        /* 포함한 Medusa 헤드 구조", the note under the p_k      */
+                        /* equation: W_head^(k) may be the frozen W_lm_head.     */
 } medusa_cfg;
 
 /* Node count N of the configured tree. Host only; `N` is a host pointer. */
@@ -102,7 +107,9 @@ MEDUSA_API int medusa_workspace_size(const medusa_cfg* cfg, size_t* bytes);
  *   h      [B][d] elt          backbone last hidden state
  *   W      [K][d][d] elt       W[k][o][i]: residual-layer weight, input i -> output o
  *   bias   [K][d] elt          b_k, may be NULL (zero bias)
- *   U      [K][V][d] elt       U[k][v][i]: vocab projection of head k
+ *   U      [K][V][d] elt       U[k][v][i]: vocab projection of head k; with
+ *                              cfg->shared_vocab, [V][d]: one projection for every
+ *                              head (its weights are streamed once for all heads)
  *   logits [B][K][V] float     z_k per sequence; may be NULL in MEDUSA_GREEDY mode
  *                              (then kept in the workspace). Needed as
  *                              `head_logits` by medusa_verify in MEDUSA_REJECTION.

@@ -34,17 +34,18 @@ class Cfg(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("d", ctypes.c_int32), ("V", ctypes.c_int32), ("K", ctypes.c_int32),
                 ("branching", ctypes.c_int32 * 8), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
                 ("D", ctypes.c_int32), ("L_cap", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("mode", ctypes.c_int32), ("temperature", ctypes.c_float)]
+                ("mode", ctypes.c_int32), ("temperature", ctypes.c_float), ("shared_vocab", ctypes.c_int32)]
 
 
 def make_cfg(B: int, d: int, V: int, branching: Sequence[int], Hq: int, Hkv: int, D: int, L_cap: int,
-             dtype: int, mode: int, temperature: float = 1.0) -> Cfg:
+             dtype: int, mode: int, temperature: float = 1.0, shared_vocab: bool = False) -> Cfg:
     c = Cfg()
     c.B, c.d, c.V, c.K = B, d, V, len(branching)
     for i, s in enumerate(branching):
         c.branching[i] = int(s)
     c.Hq, c.Hkv, c.D, c.L_cap = Hq, Hkv, D, L_cap
     c.dtype, c.mode, c.temperature = dtype, mode, float(temperature)
+    c.shared_vocab = 1 if shared_vocab else 0
     return c
 
 

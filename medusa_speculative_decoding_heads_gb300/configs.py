@@ -39,6 +39,7 @@ class Workload:
     target_corr: float                # correlation of target logits with head logits
     compact: bool                     # KV compaction listed for the workload
     w_sigma: float = 0.02             # std of W_k and of the vocab projections
+    shared_vocab: bool = False        # one vocab projection U for every head (U is [V][d])
     note: str = ""
 
     @property
@@ -92,6 +93,14 @@ WORKLOADS = {
 }
 
 ORDER = ["tiny_fp32", "vicuna7b_b1", "vicuna13b_b8", "vicuna33b_b16", "gqa7b_b32"]
+
+# The same steps with one frozen vocab projection shared by every head.
+for _base in ("vicuna7b_b1", "vicuna13b_b8"):
+    _w = WORKLOADS[_base]
+    WORKLOADS[_base + "_shared"] = Workload(**dict(
+        {k: getattr(_w, k) for k in _w.__dataclass_fields__}, name=_base + "_shared", shared_vocab=True,
+        note=_w.note + "; every head projects with one shared (frozen LM-head) vocab matrix"))
+SHARED = ["vicuna7b_b1_shared", "vicuna13b_b8_shared"]
 
 
 def get(name: str) -> Workload:

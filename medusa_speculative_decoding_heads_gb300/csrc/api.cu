@@ -37,6 +37,7 @@ int check_cfg(const medusa_cfg* c) {
   if (c->D != 64 && c->D != 128) return MEDUSA_ERR_UNSUPPORTED;
   if (c->L_cap < n) return MEDUSA_ERR_CAPACITY;
   if (c->mode == MEDUSA_REJECTION && !(c->temperature > 0.f)) return MEDUSA_ERR_INVALID_ARG;
+  if (c->shared_vocab != 0 && c->shared_vocab != 1) return MEDUSA_ERR_INVALID_ARG;
   return MEDUSA_OK;
 }
 

@@ -275,9 +275,9 @@ constexpr int kF32DChunk = 1024;
 
 template <bool RESIDUAL>
 __global__ void __launch_bounds__(256)
-heads_f32_kernel(const float* __restrict__ A, int rows, int d, const float* __restrict__ X, size_t x_b_stride,
-                 size_t x_group_stride, int B, int G, float* __restrict__ out, const float* __restrict__ h,
-                 const float* __restrict__ bias) {
+heads_f32_kernel(const float* __restrict__ A, size_t a_group_stride, int rows, int d, const float* __restrict__ X,
+                 size_t x_b_stride, size_t x_group_stride, int B, int G, float* __restrict__ out,
+                 const float* __restrict__ h, const float* __restrict__ bias) {
   pdl_wait();
   pdl_trigger();
   __shared__ float xs[kF32B][kF32DChunk];
@@ -304,7 +304,7 @@ heads_f32_kernel(const float* __restrict__ A, int rows, int d, const float* __re
       for (int r = 0; r < kF32Rows; ++r) {
         int row = row0 + r;
         if (row >= rows) continue;
-        const float* ar = A + ((size_t)g * rows + row) * d + k0;
+        const float* ar = A + (size_t)g * a_group_stride + (size_t)row * d + k0;
         for (int k = lane; k < kn; k += 32) {
           float a = ar[k];
 #pragma unroll
@@ -611,6 +611,7 @@ cudaError_t launch_heads(const medusa_cfg& c, const void* h, const void* W, cons
   char* base = static_cast<char*>(ws);
   const int B = c.B, d = c.d, V = c.V, K = c.K;
   float* z = logits ? logits : reinterpret_cast<float*>(base + p.zbuf);
+  const size_t u_stride = c.shared_vocab ? 0 : (size_t)V * d;   // elements between heads' vocab projections
 
   if (heads_tc_supported(c)) {
     cudaError_t e = launch_heads_tc(c, h, W, bias, U, z, base + p.tc, st);
@@ -631,7 +632,7 @@ cudaError_t launch_heads(const medusa_cfg& c, const void* h, const void* W, cons
                                                         xp1, 0, cps1, part1, (size_t)B * K * d, B, K);          \
     launch_pdl(residual_pack_kernel<NT_>, 256, 256, 0, st, part1, p.ksplit1, static_cast<const uint16_t*>(h),           \
                                                    static_cast<const uint16_t*>(bias), xp2, B, K, d);           \
-    launch_pdl(heads_mma_kernel<NT_, 2>, g2, kWarps * 32, 0, st, static_cast<const uint16_t*>(U), (size_t)V * d, V, d,   \
+    launch_pdl(heads_mma_kernel<NT_, 2>, g2, kWarps * 32, 0, st, static_cast<const uint16_t*>(U), u_stride, V, d,      \
                                                         xp2, xp2_group, nchunks, z, 0, B, K);                   \
     note_launches(4);                                                                                            \
   } while (0)
@@ -642,12 +643,14 @@ cudaError_t launch_heads(const medusa_cfg& c, const void* h, const void* W, cons
   } else {
     float* r = reinterpret_cast<float*>(base + p.xp2);
     dim3 g1((d + 32 - 1) / 32, K);
-    launch_pdl(heads_f32_kernel<true>, g1, 256, 0, st, static_cast<const float*>(W), d, d, static_cast<const float*>(h),
+    launch_pdl(heads_f32_kernel<true>, g1, 256, 0, st, static_cast<const float*>(W), (size_t)d * d, d, d,
+                                               static_cast<const float*>(h),
                                                (size_t)d, 0, B, K, r, static_cast<const float*>(h),
                                                static_cast<const float*>(bias));
     note_launches(1);
     dim3 g2((V + 32 - 1) / 32, K);
-    launch_pdl(heads_f32_kernel<false>, g2, 256, 0, st, static_cast<const float*>(U), V, d, r, (size_t)K * d, (size_t)d, B,
+    launch_pdl(heads_f32_kernel<false>, g2, 256, 0, st, static_cast<const float*>(U), u_stride, V, d, r, (size_t)K * d,
+                                                (size_t)d, B,
                                                 K, z, nullptr, nullptr);
     note_launches(1);
   }

@@ -42,7 +42,8 @@ constexpr int kRowsTile = 128;
 constexpr int kChunkK = 64;
 constexpr int kATile = kRowsTile * 128;     // 16 KB: 128 rows x 64 bf16
 constexpr int kSmemBudget = 200 * 1024;
-constexpr uint32_t kAccCols = 64;           // columns per TMEM accumulator (N <= 64)
+// Columns per TMEM accumulator (two accumulators; the allocation is a power of two).
+__host__ __device__ constexpr uint32_t acc_cols(int ncol) { return ncol <= 64 ? 64u : (ncol <= 128 ? 128u : 256u); }
 
 template <int NCOL>
 struct HeadsGeom {
@@ -90,11 +91,22 @@ __device__ __forceinline__ bool unit_of(int i, int G, int tiles, int nchunks, in
 // out[slot][b][g][r] = sum_k A[g*rows + r][k] * X[g*x_rows + col(b)][k] over the
 // unit's k range; col(b) = b (+ NB for the lo part when HILO). The residual
 // layer (!HILO) uses the stream-K schedule, the vocab projection round robin.
-template <int NCOL, bool HILO>
+//
+// The X block of a unit holds nxh head blocks of HB columns each (one, except
+// when all heads share one vocab projection: then one MMA of N = nxh * HB
+// columns, rounded up with zero rows, serves every head from a single stream
+// of the weights). Within a head block, column j < HB / 2 is sequence j's hi
+// part and j + HB / 2 its lo part (HILO), or column j is sequence j (!HILO).
+// Output element (slot, b, head, r) goes to
+// out + slot * out_split_stride + b * bstride + (g + head) * hstride + r.
+// a_head_rows is the row offset of head g in A (0 when the heads share A).
+template <int NCOL, bool HILO, int HB>
 __global__ void __launch_bounds__(192, 1)
 heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmX, int rows, int G,
-                int x_rows, int nchunks, int nk, int ksplit, int B, float* __restrict__ out,
-                size_t out_split_stride) {
+                int a_head_rows, int x_rows, int nchunks, int nk, int ksplit, int B, int nxh, float* __restrict__ out,
+                size_t out_split_stride, size_t bstride, size_t hstride) {
+  constexpr uint32_t kAccCols = acc_cols(NCOL);
+  static_assert(NCOL < 64 ? HB == NCOL : 64 % HB == 0, "head blocks must tile the 64-column passes");
   pdl_trigger();
   using Geo = HeadsGeom<NCOL>;
   constexpr int S = Geo::kStages;
@@ -121,7 +133,7 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
     tc::mbar_fence_init();
   }
-  if (warp == 4) tc::tmem_alloc(&tmem_slot, 2 * kAccCols);
+  if (warp == 4) tc::tmem_alloc(&tmem_slot, 2 * kAccCols);   // 128, 256 or 512 columns
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -132,7 +144,8 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // stale data; the real loads come after the wait below).
     int n = 0, g, t, c0, c1, slot;
     for (int i = 0; n < S && unit_of<kStream>(i, G, tiles, nchunks, nk, ksplit, g, t, c0, c1, slot); ++i)
-      for (int c = c0; c < c1 && n < S; ++c, ++n) tc::tma_prefetch_2d(&tmA, c * kChunkK, g * rows + t * kRowsTile);
+      for (int c = c0; c < c1 && n < S; ++c, ++n)
+        tc::tma_prefetch_2d(&tmA, c * kChunkK, g * a_head_rows + t * kRowsTile);
   }
   pdl_wait();   // the setup above overlaps the previous kernel's tail; no global access before this
 
@@ -149,7 +162,7 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             break;
           }
           tc::mbar_arrive_expect(&full[s], kATile + Geo::kXTile);
-          tc::tma_load_2d(As + s * kATile, &tmA, c * kChunkK, g * rows + t * kRowsTile, &full[s]);
+          tc::tma_load_2d(As + s * kATile, &tmA, c * kChunkK, g * a_head_rows + t * kRowsTile, &full[s]);
           tc::tma_load_2d(Xs + s * Geo::kXTile, &tmX, c * kChunkK, g * x_rows, &full[s]);
         }
       }
@@ -194,23 +207,31 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const bool ok = tc::mbar_wait(&acc_full[a], (ui >> 1) & 1, err, 16);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc::fence_after();
-      uint32_t v[64];
-      tc::tmem_ld32(tmem + a * kAccCols + lane_base, v);
-      if (NCOL > 32) tc::tmem_ld32(tmem + a * kAccCols + lane_base + 32, v + 32);
-      tc::tmem_wait_ld();
-      tc::fence_before();
-      tc::mbar_arrive(&acc_empty[a]);
       const int r = t * kRowsTile + i;
-      if (r < rows) {
-        float* o = out + (size_t)slot * out_split_stride + (size_t)g * rows + r;
-        const size_t bstride = (size_t)G * rows;
-        constexpr int kCols = HILO ? NCOL / 2 : NCOL;   // batch columns (lo part follows when HILO)
+      float* ob = out + (size_t)slot * out_split_stride + (size_t)g * hstride + r;
+      constexpr int kWin = NCOL < 64 ? NCOL : 64;       // columns per pass (two 32-column loads)
+      constexpr int kWins = (NCOL + 63) / 64;
+      constexpr int kHalf = HILO ? HB / 2 : HB;         // sequences per head block
+      constexpr int kPerWin = NCOL < 64 ? 1 : 64 / HB;  // head blocks per pass
+#pragma unroll 1
+      for (int w = 0; w < kWins; ++w) {
+        uint32_t v[64];
+        tc::tmem_ld32(tmem + a * kAccCols + lane_base + 64 * w, v);
+        if (kWin > 32) tc::tmem_ld32(tmem + a * kAccCols + lane_base + 64 * w + 32, v + 32);
+        tc::tmem_wait_ld();
+        if (w == kWins - 1) {   // the accumulator is free once its last columns are in registers
+          tc::fence_before();
+          tc::mbar_arrive(&acc_empty[a]);
+        }
+        if (r < rows) {
 #pragma unroll
-        for (int b = 0; b < kCols; ++b) {
-          if (b < B) {
-            float x = __uint_as_float(v[b]);
-            if (HILO) x += __uint_as_float(v[kCols + b]);
-            o[(size_t)b * bstride] = x;
+          for (int j = 0; j < kWin; ++j) {
+            const int cc = j % HB, head = w * kPerWin + j / HB;
+            if (cc < kHalf && cc < B && head < nxh) {
+              float x = __uint_as_float(v[j]);
+              if (HILO) x += __uint_as_float(v[j + kHalf]);
+              ob[(size_t)cc * bstride + (size_t)head * hstride] = x;
+            }
           }
         }
       }
@@ -280,20 +301,21 @@ __global__ void residual_pack_tc_kernel(const float* __restrict__ part, int tile
   }
 }
 
-template <int NCOL, bool HILO>
-cudaError_t run_gemv(const CUtensorMap& tmA, const CUtensorMap& tmX, int rows, int G, int x_rows, int nchunks, int ks,
-                     int B, float* out, size_t out_split_stride, int num_sms, cudaStream_t st) {
+template <int NCOL, bool HILO, int HB>
+cudaError_t run_gemv(const CUtensorMap& tmA, const CUtensorMap& tmX, int rows, int G, int a_head_rows, int x_rows,
+                     int nchunks, int ks, int B, int nxh, float* out, size_t out_split_stride, size_t bstride,
+                     size_t hstride, int num_sms, cudaStream_t st) {
   using Geo = HeadsGeom<NCOL>;
   const int nk = (nchunks + ks - 1) / ks;   // round robin: ks divides the chunks so that no split is empty
   const int tiles = (rows + kRowsTile - 1) / kRowsTile;
   // stream-K (!HILO): one CTA per SM, or one per chunk when there are fewer chunks
   const long long nunits = HILO ? (long long)G * tiles * ks : (long long)G * tiles * nchunks;
-  cudaError_t e = cudaFuncSetAttribute(heads_tc_kernel<NCOL, HILO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(heads_tc_kernel<NCOL, HILO, HB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Geo::kSmem);
   if (e != cudaSuccess) return e;
   const int grid = nunits < num_sms ? (int)nunits : num_sms;
-  launch_pdl(heads_tc_kernel<NCOL, HILO>, grid, 192, Geo::kSmem, st, tmA, tmX, rows, G, x_rows, nchunks, nk, ks, B, out,
-                                                              out_split_stride);
+  launch_pdl(heads_tc_kernel<NCOL, HILO, HB>, grid, 192, Geo::kSmem, st, tmA, tmX, rows, G, a_head_rows, x_rows,
+             nchunks, nk, ks, B, nxh, out, out_split_stride, bstride, hstride);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -316,10 +338,18 @@ static int stream_ctas(const medusa_cfg& c) {
   return (int)(T < sm_count() ? T : sm_count());
 }
 
+// MMA width of the shared-projection GEMV: all K head blocks of NCOL2 columns
+// in one B operand, rounded up to 64, 128 or 256 (0: too wide for one MMA).
+static int shared_block(int K, int ncol2) {
+  const int n = K * ncol2;
+  return n <= 64 ? 64 : (n <= 128 ? 128 : (n <= 256 ? 256 : 0));
+}
+
 // Workspace layout of the tensor-core heads path.
 HeadsTcPlan plan_heads_tc(const medusa_cfg& c) {
   HeadsTcPlan p{};
   p.NB = c.B <= 8 ? 8 : (c.B + 7) / 8 * 8;               // batch columns per part (hi or lo)
+  if (c.shared_vocab) p.NB = c.B <= 8 ? 8 : (c.B <= 16 ? 16 : 32);   // head blocks of 16, 32 or 64 columns
   p.NCOL1 = c.B <= 16 ? 16 : 32;                          // d x d layer: h only
   p.NCOL2 = 2 * p.NB;                                     // vocab projection: hi and lo
   // partial-sum slots of the residual layer: at most the CTAs whose equal
@@ -335,7 +365,10 @@ HeadsTcPlan plan_heads_tc(const medusa_cfg& c) {
     off = align_up(off + bytes, 256);
     return o;
   };
-  p.x2 = take((size_t)c.K * p.NCOL2 * c.d * 2);
+  // hi/lo vectors [K][NCOL2][d]; with a shared projection, padded to the MMA's N
+  // rows (the rows past K * NCOL2 only feed output columns that are never read)
+  const int xrows = c.shared_vocab && shared_block(c.K, p.NCOL2) ? shared_block(c.K, p.NCOL2) : c.K * p.NCOL2;
+  p.x2 = take((size_t)xrows * c.d * 2);
   p.part1 = take((size_t)p.slots1 * c.B * c.K * c.d * 4);
   p.total = off;
   return p;
@@ -355,7 +388,7 @@ cudaError_t launch_heads_tc(const medusa_cfg& c, const void* h, const void* W, c
       // the residual layer reads h itself: rows B..NCOL1-1 of each box lie past
       // the tensor and arrive as zeros
       !encode_tmap_2d_bf16(&tmX1, h, (uint64_t)B, d, (uint64_t)d * 2, kChunkK, p.NCOL1) ||
-      !encode_tmap_2d_bf16(&tmU, U, (uint64_t)K * V, d, (uint64_t)d * 2, kChunkK, kRowsTile) ||
+      !encode_tmap_2d_bf16(&tmU, U, (uint64_t)(c.shared_vocab ? 1 : K) * V, d, (uint64_t)d * 2, kChunkK, kRowsTile) ||
       !encode_tmap_2d_bf16(&tmX2, x2, (uint64_t)K * p.NCOL2, d, (uint64_t)d * 2, kChunkK, p.NCOL2))
     return cudaErrorInvalidValue;
   const int sms = sm_count();
@@ -363,19 +396,44 @@ cudaError_t launch_heads_tc(const medusa_cfg& c, const void* h, const void* W, c
   const int P1 = stream_ctas(c);
   if (((long long)K * ((d + kRowsTile - 1) / kRowsTile) * nchunks + 1) * P1 >= (1LL << 32)) return cudaErrorInvalidValue;
   cudaError_t e = p.NCOL1 == 16
-                      ? run_gemv<16, false>(tmW, tmX1, d, K, 0, nchunks, 1, B, part1, (size_t)B * K * d, P1, st)
-                      : run_gemv<32, false>(tmW, tmX1, d, K, 0, nchunks, 1, B, part1, (size_t)B * K * d, P1, st);
+                      ? run_gemv<16, false, 16>(tmW, tmX1, d, K, d, 0, nchunks, 1, B, 1, part1, (size_t)B * K * d,
+                                                (size_t)K * d, (size_t)d, P1, st)
+                      : run_gemv<32, false, 32>(tmW, tmX1, d, K, d, 0, nchunks, 1, B, 1, part1, (size_t)B * K * d,
+                                                (size_t)K * d, (size_t)d, P1, st);
   if (e != cudaSuccess) return e;
+  const bool shared = c.shared_vocab && shared_block(K, p.NCOL2);
   const int rp_blocks = (int)(((size_t)K * p.NB * (d / 4) + 255) / 256);
   launch_pdl(residual_pack_tc_kernel, rp_blocks < 1024 ? rp_blocks : 1024, 256, 0, st, part1,
              (d + kRowsTile - 1) / kRowsTile, nchunks, P1, static_cast<const uint16_t*>(h),
              static_cast<const uint16_t*>(bias), x2, B, p.NB, K, d);
   note_launches(1);
+  const size_t bs = (size_t)K * V;   // z [B][K][V]
+  if (shared) {
+    // one stream of U for all heads: X = every head's hi/lo vectors, N = K * NCOL2 rounded up
+    const int nt = shared_block(K, p.NCOL2);
+    CUtensorMap tmXs;
+    if (!encode_tmap_2d_bf16(&tmXs, x2, (uint64_t)nt, d, (uint64_t)d * 2, kChunkK, nt))
+      return cudaErrorInvalidValue;
+#define MEDUSA_SHARED(NT, HB) \
+  if (nt == NT && p.NCOL2 == HB) return run_gemv<NT, true, HB>(tmU, tmXs, V, 1, 0, 0, nchunks, 1, B, K, z, 0, bs, V, sms, st)
+    MEDUSA_SHARED(64, 16);
+    MEDUSA_SHARED(128, 16);
+    MEDUSA_SHARED(64, 32);
+    MEDUSA_SHARED(128, 32);
+    MEDUSA_SHARED(256, 32);
+    MEDUSA_SHARED(64, 64);
+    MEDUSA_SHARED(128, 64);
+    MEDUSA_SHARED(256, 64);
+#undef MEDUSA_SHARED
+    return cudaErrorInvalidValue;
+  }
+  // one vocab projection per head (or a shared one too wide for one block: head g reads rows g * a_rows of U)
+  const int a_rows = c.shared_vocab ? 0 : V;
   switch (p.NCOL2) {
-    case 16: return run_gemv<16, true>(tmU, tmX2, V, K, p.NCOL2, nchunks, 1, B, z, 0, sms, st);
-    case 32: return run_gemv<32, true>(tmU, tmX2, V, K, p.NCOL2, nchunks, 1, B, z, 0, sms, st);
-    case 48: return run_gemv<48, true>(tmU, tmX2, V, K, p.NCOL2, nchunks, 1, B, z, 0, sms, st);
-    default: return run_gemv<64, true>(tmU, tmX2, V, K, p.NCOL2, nchunks, 1, B, z, 0, sms, st);
+    case 16: return run_gemv<16, true, 16>(tmU, tmX2, V, K, a_rows, p.NCOL2, nchunks, 1, B, 1, z, 0, bs, V, sms, st);
+    case 32: return run_gemv<32, true, 32>(tmU, tmX2, V, K, a_rows, p.NCOL2, nchunks, 1, B, 1, z, 0, bs, V, sms, st);
+    case 48: return run_gemv<48, true, 48>(tmU, tmX2, V, K, a_rows, p.NCOL2, nchunks, 1, B, 1, z, 0, bs, V, sms, st);
+    default: return run_gemv<64, true, 64>(tmU, tmX2, V, K, a_rows, p.NCOL2, nchunks, 1, B, 1, z, 0, bs, V, sms, st);
   }
 }
 

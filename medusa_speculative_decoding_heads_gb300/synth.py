@@ -148,7 +148,7 @@ def make_step_inputs(w: Workload, seed: int, device="cpu", with_bias: bool = Fal
     h = normal(gen, (B, d), 1.0, w.dtype, dev)
     W = normal(gen, (K, d, d), w.w_sigma, w.dtype, dev)
     bias = normal(gen, (K, d), bias_sigma, w.dtype, dev) if with_bias else None
-    U = normal(gen, (K, V, d), w.w_sigma, w.dtype, dev)
+    U = normal(gen, (V, d) if w.shared_vocab else (K, V, d), w.w_sigma, w.dtype, dev)
     L = committed_lengths(seed, B, *w.L_range)
     L_cap = cache_capacity(L, N)
     Q = normal(gen, (B, N, w.Hq, w.D), 1.0, w.dtype, dev)

@@ -79,11 +79,14 @@ def medusa_heads(h: np.ndarray, W: np.ndarray, b: Optional[np.ndarray], U: np.nd
 
     Layouts: h [B][d]; W [K][d][d] with W[k][o][i] the weight from input i to
     output o (the nn.Linear convention); b [K][d] or None; U [K][V][d] with
-    U[k][v][i] the weight from feature i to token v.
+    U[k][v][i] the weight from feature i to token v, or U [V][d]: one vocab
+    projection shared by every head (the same section notes that W_head^(k)
+    may be the base model's frozen unembedding W_lm_head, kept as is).
     Returns r [B][K][d] (R5: unrounded) and logits z [B][K][V].
     """
     B, d = h.shape
-    K, V = U.shape[0], U.shape[1]
+    K = W.shape[0]
+    V = U.shape[-2]
     r = np.empty((B, K, d), dtype=np.float64)
     z = np.empty((B, K, V), dtype=np.float64)
     for k in range(K):
@@ -91,7 +94,8 @@ def medusa_heads(h: np.ndarray, W: np.ndarray, b: Optional[np.ndarray], U: np.nd
         if b is not None:
             pre = pre + b[k][None, :]
         r[:, k, :] = h + silu(pre)
-        z[:, k, :] = r[:, k, :] @ U[k].T
+        Uk = U if U.ndim == 2 else U[k]
+        z[:, k, :] = r[:, k, :] @ Uk.T
     return r, z
 
 

@@ -72,7 +72,7 @@ def check_heads(w, si, st, rows=None):
     for k in sorted({k for _, k in pairs}):
         Wk = f64(si.W[k:k + 1])
         bk = None if si.bias is None else f64(si.bias[k:k + 1])
-        Uk = f64(si.U[k:k + 1])
+        Uk = f64(si.U) if w.shared_vocab else f64(si.U[k:k + 1])
         bs = sorted({b for b, kk in pairs if kk == k})
         _, z = O.medusa_heads(h[bs], Wk, bk, Uk)
         for j, b in enumerate(bs):
@@ -112,7 +112,33 @@ def test_heads_batch_tiles(B):
     check_heads(w, si, st)
 
 
-@pytest.mark.parametrize("name", NAMES[1:])
+@pytest.mark.parametrize("base,B,d,V", [("vicuna7b_b1", 1, 320, 700), ("vicuna7b_b1", 9, 320, 700),
+                                        ("vicuna7b_b1", 17, 320, 700), ("vicuna7b_b1", 32, 320, 700),
+                                        ("vicuna13b_b8", 3, 320, 700), ("vicuna13b_b8", 16, 320, 700),
+                                        ("vicuna13b_b8", 32, 320, 700), ("tiny_fp32", 2, None, None),
+                                        ("vicuna7b_b1", 1, 128, 19585), ("vicuna7b_b1", 17, 128, 19600),
+                                        ("vicuna13b_b8", 8, 192, 30000)])
+def test_heads_shared_vocab(base, B, d, V):
+    """One vocab projection for every head: one weight stream serving all heads' columns
+    (head blocks of 16, 32 and 64 columns in MMAs of 64, 128 and 256), the per-head
+    path when all heads do not fit one MMA (K = 5 with B = 32) and the float32 path.
+    The larger vocabularies put more than one 128-row tile on every SM, one of them
+    with V not a multiple of 4 (ragged last tile, scalar top-s loads)."""
+    dev = gpu_ready()
+    w0 = configs.get(base)
+    kw = dict(B=B, shared_vocab=True)
+    if base != "tiny_fp32":
+        kw.update(d=d, V=V, L_range=(40, 40), Hq=2, Hkv=2)
+    w = configs.scaled(w0, **kw)
+    si = synth.make_step_inputs(w, seed=B + 100, device=dev, with_bias=True)
+    assert tuple(si.U.shape) == (w.V, w.d)
+    st = DeviceStep(w, w.modes[0], si.L_cap, dev)
+    st.heads(si.h, si.W, si.bias, si.U)
+    torch.cuda.synchronize()
+    check_heads(w, si, st)
+
+
+@pytest.mark.parametrize("name", NAMES[1:] + configs.SHARED)
 def test_heads_full_size_sampled(name):
     dev = gpu_ready()
     w = configs.get(name)
@@ -384,7 +410,7 @@ def test_kv_compact_bit_exact(name):
 
 
 # --------------------------------------------------------------------------- whole step
-@pytest.mark.parametrize("name", NAMES)
+@pytest.mark.parametrize("name", NAMES + configs.SHARED)
 def test_step_end_to_end_small(name):
     """The five calls in order on one stream against the oracle's step on the same inputs."""
     dev = gpu_ready()

@@ -94,3 +94,35 @@ def test_top_s_ties_to_lower_index_and_flag():
     assert list(idx) == [1, 3] and near
     idx, near = O.top_s(np.array([0.0, 5.0, 3.0, 4.0]), 2)
     assert list(idx) == [1, 3] and not near
+
+
+def test_shared_vocab_hand_example():
+    """Two heads, different residual layers, one shared vocab projection U [V][d]
+    (the frozen LM-head option): each head's logits are U r_k, summed by hand."""
+    h = np.array([[2.0, -1.0]])
+    W = np.array([[[1.0, 0.0], [0.0, 0.0]],      # head 0: out 0 <- in 0
+                  [[0.0, 0.0], [0.0, -3.0]]])    # head 1: out 1 <- -3 in 1
+    U = np.array([[1.0, 2.0],
+                  [0.0, -1.0],
+                  [3.0, 1.0]])
+    r, z = O.medusa_heads(h, W, None, U)
+    sig = lambda v: 1.0 / (1.0 + math.exp(-v))
+    r0 = [2.0 + 2.0 * sig(2.0), -1.0 + 0.0]
+    r1 = [2.0 + 0.0, -1.0 + 3.0 * sig(3.0)]
+    for k, rk in enumerate((r0, r1)):
+        np.testing.assert_allclose(r[0, k], rk, rtol=1e-14)
+        want = [sum(U[v][i] * rk[i] for i in range(2)) for v in range(3)]
+        np.testing.assert_allclose(z[0, k], want, rtol=1e-14)
+
+
+def test_shared_vocab_zero_residual_is_one_gemv_for_all_heads():
+    """W = 0: every head's logits are the same U h (brute-force loops)."""
+    rng = np.random.default_rng(7)
+    B, K, d, V = 2, 3, 5, 6
+    h = rng.standard_normal((B, d))
+    U = rng.standard_normal((V, d))
+    _, z = O.medusa_heads(h, np.zeros((K, d, d)), None, U)
+    for b in range(B):
+        want = [sum(U[v, i] * h[b, i] for i in range(d)) for v in range(V)]
+        for k in range(K):
+            np.testing.assert_allclose(z[b, k], want, rtol=1e-12)
