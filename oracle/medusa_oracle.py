@@ -162,6 +162,44 @@ def tree_layout(branching: Sequence[int]):
             "first_child": np.array(first_child, dtype=np.int64)}
 
 
+def tree_layout_from_paths(paths: Sequence[Sequence[int]], branching: Sequence[int]):
+    """Node order and parent links of a pruned candidate tree given by its nodes' rank paths.
+
+    [MEDUSA-ARCH] runs its benchmarks with 4 heads and 64 tree branches
+    ("벤치마크 실측 지표: 도메인별 속도 향상 및 수용률") and calls a topology of
+    about 32-64 nodes the usual optimum ("트리 크기(Tree Size)와 검증 오버헤드의
+    균형"): a subset of the Cartesian tree rather than all of it. Reading (R13):
+    the tree is given as the set of its non-root nodes' rank paths (i_1, ..., i_d)
+    with 0 <= i_e < s_e, closed under prefixes; node order is R2's (breadth
+    first, lexicographic by rank path), so each node's children are contiguous
+    and in rank order, and a node's token is head d's candidate i_d (R3). The
+    full Cartesian product gives back tree_layout(branching).
+    Returns the same dict as tree_layout.
+    """
+    K = len(branching)
+    ps = sorted({tuple(int(i) for i in p) for p in paths}, key=lambda p: (len(p), p))
+    for p in ps:
+        if not 1 <= len(p) <= K:
+            raise ValueError(f"path {p}: depth outside 1..{K}")
+        if any(not 0 <= p[e] < branching[e] for e in range(len(p))):
+            raise ValueError(f"path {p}: rank outside the head's top-s")
+        if len(p) > 1 and p[:-1] not in ps:
+            raise ValueError(f"path {p}: its prefix is not a node")
+    ordered = [()] + ps
+    index = {p: n for n, p in enumerate(ordered)}
+    N = len(ordered)
+    parent = [-1] + [index[p[:-1]] for p in ordered[1:]]
+    depth = [len(p) for p in ordered]
+    rank = [p[-1] if p else 0 for p in ordered]
+    first_child = []
+    for n in range(N):
+        kids = [c for c in range(N) if parent[c] == n]
+        first_child.append(min(kids) if kids else -1)
+    return {"N": N, "paths": ordered, "parent": np.array(parent, dtype=np.int64),
+            "depth": np.array(depth, dtype=np.int64), "rank": np.array(rank, dtype=np.int64),
+            "first_child": np.array(first_child, dtype=np.int64)}
+
+
 def ancestor_mask(parent: np.ndarray) -> np.ndarray:
     """mask[i][j] = 1 iff j is an ancestor of i or j == i.
 
@@ -191,14 +229,15 @@ def mask_bits(mask: np.ndarray) -> np.ndarray:
 
 
 def tree_build(branching: Sequence[int], root_token: np.ndarray, topk: np.ndarray,
-               L: np.ndarray, L_cap: Optional[int] = None):
+               L: np.ndarray, L_cap: Optional[int] = None, paths: Optional[Sequence[Sequence[int]]] = None):
     """Tree arrays, per-sequence tokens and position ids (R1-R3, R7).
 
     tokens[b][0] = root_token[b]; tokens[b][n] = topk[b][depth-1][rank] (R3);
     pos[b][n] = L[b] + depth[n] (R7). flags[b] gets FLAG_CAPACITY when
-    L[b] + N exceeds L_cap.
+    L[b] + N exceeds L_cap. `paths` selects a pruned tree (R13) instead of the
+    full Cartesian one.
     """
-    lay = tree_layout(branching)
+    lay = tree_layout(branching) if paths is None else tree_layout_from_paths(paths, branching)
     N = lay["N"]
     B = root_token.shape[0]
     mask = ancestor_mask(lay["parent"])
