@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=configs.ORDER + configs.SHARED)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=configs.ORDER + configs.SHARED + configs.PRUNED)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -169,7 +169,7 @@ def oracle_inputs_from(si, tl):
 def oracle_step(O, w, mode, x):
     r, z = O.medusa_heads(x["h"], x["W"], x["b"], x["U"])
     topk, _ = O.heads_top_s(z, w.branching)
-    tree = O.tree_build(w.branching, x["root"], topk, x["L"], x["L_cap"])
+    tree = O.tree_build(w.branching, x["root"], topk, x["L"], x["L_cap"], paths=w.tree_paths)
     O.tree_attention(x["Q"], x["Kc"], x["Vc"], x["L"], tree["mask"], w.Hq, w.Hkv)
     ver = O.verify_batch(mode, tree, x["tl"], w.K, head_logits=z, u_acc=x["u_acc"], u_res=x["u_res"],
                          T=w.temperature)
@@ -209,6 +209,7 @@ def workload_config(w, L, mode, world):
             "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "L": [int(x) for x in L][:4],
             "L_sum": int(np.sum(L)), "mode": "greedy" if mode == GREEDY else "rejection",
             "temperature": w.temperature if mode == REJECTION else None, "shared_vocab": w.shared_vocab,
+            "tree": "pruned" if w.tree_paths is not None else "cartesian",
             "l2": f"inputs larger than L2 ({(weights + kv) / 1e9:.2f} GB of weights and KV per step)",
             "parallelism": f"replicas x{world}"}
 
@@ -258,7 +259,9 @@ def make_targets(w, si, dev, mode, seed, via_library=True):
         from oracle import medusa_oracle as O
         f = lambda t: t.detach().to("cpu", torch.float32).double().numpy()
         _, z = O.medusa_heads(f(si.h), f(si.W), None if si.bias is None else f(si.bias), f(si.U))
-        zhat, depth = torch.from_numpy(z).float(), O.tree_layout(w.branching)["depth"]
+        lay = (O.tree_layout(w.branching) if w.tree_paths is None
+               else O.tree_layout_from_paths(w.tree_paths, w.branching))
+        zhat, depth = torch.from_numpy(z).float(), lay["depth"]
     return synth.target_logits(w, seed, device=dev, zhat=zhat, depth=depth)
 
 

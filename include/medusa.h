@@ -32,8 +32,9 @@
  *     per-sequence `flags` word and the affected sequence is skipped.
  *   - Layouts are dense row-major with the shapes given; "elt" is float when
  *     cfg->dtype == MEDUSA_F32 and bf16 (uint16 bit pattern) when MEDUSA_BF16.
- *   - N = 1 + sum_{k=1..K} prod_{j<=k} s_j is the node count (N <= 128),
- *     s_max = max_k s_k (<= 8), K <= 8.
+ *   - N = 1 + sum_{k=1..K} prod_{j<=k} s_j is the node count of the Cartesian
+ *     tree, or cfg->tree_nodes for a pruned tree (N <= 128); s_max = max_k s_k
+ *     (<= 8), K <= 8.
  *   - Tree node order: breadth first; within a depth, lexicographic in the
  *     path of sibling ranks (first rank most significant). Node 0 is the root,
  *     which is the already committed next token of each sequence.
@@ -93,6 +94,18 @@ typedef struct {
                         /* head), "Medusa 심층 아키텍처", section "잔차 블록을     */
                         /* 포함한 Medusa 헤드 구조", the note under the p_k      */
                         /* equation: W_head^(k) may be the frozen W_lm_head.     */
+  int32_t tree_nodes;   /* 0: the full Cartesian tree of branching[]. 1..128: a   */
+                        /* pruned tree of that many nodes (node 0 = root), given  */
+                        /* by tree_parent/tree_rank in breadth-first order,       */
+                        /* lexicographic in the rank path within a depth (so a    */
+                        /* node's children are contiguous and in rank order).     */
+                        /* "Medusa 심층 아키텍처", sections "벤치마크 실측 지표"  */
+                        /* (4 heads, 64 tree branches) and "트리 크기(Tree Size)와 */
+                        /* 검증 오버헤드의 균형" (32-64 nodes usually best).        */
+  int16_t tree_parent[128]; /* pruned tree: parent node (-1 at the root)          */
+  uint8_t tree_rank[128];   /* pruned tree: the node's rank in its head's top-s   */
+                            /* list (< branching[depth - 1]); its token is        */
+                            /* topk[b][depth - 1][rank]                           */
 } medusa_cfg;
 
 /* Node count N of the configured tree. Host only; `N` is a host pointer. */
@@ -126,7 +139,7 @@ MEDUSA_API int medusa_heads(const medusa_cfg* cfg, const void* h, const void* W,
  *   root_token [B] int32, topk [B][K][s_max] int32, L [B] int32 (committed lengths).
  * Outputs (the first five are identical for every sequence):
  *   parent [N] int32 (-1 at the root), depth [N] int32, first_child [N] int32
- *   (-1 at depth K; children of a node are contiguous, in rank order),
+ *   (-1 at a leaf; children of a node are contiguous, in rank order),
  *   mask [N][N] uint8 (1 iff column is an ancestor of the row or the row itself),
  *   anc_bits [N][2] uint64 (bit j of word j/64 = mask[i][j]),
  *   tokens [B][N] int32 (root_token, then topk[b][depth-1][rank]),

@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from typing import Optional, Sequence
+from typing import Optional, Sequence, Tuple
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmedusa.so")
@@ -34,11 +34,15 @@ class Cfg(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("d", ctypes.c_int32), ("V", ctypes.c_int32), ("K", ctypes.c_int32),
                 ("branching", ctypes.c_int32 * 8), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
                 ("D", ctypes.c_int32), ("L_cap", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("mode", ctypes.c_int32), ("temperature", ctypes.c_float), ("shared_vocab", ctypes.c_int32)]
+                ("mode", ctypes.c_int32), ("temperature", ctypes.c_float), ("shared_vocab", ctypes.c_int32),
+                ("tree_nodes", ctypes.c_int32), ("tree_parent", ctypes.c_int16 * 128), ("tree_rank", ctypes.c_uint8 * 128)]
 
 
 def make_cfg(B: int, d: int, V: int, branching: Sequence[int], Hq: int, Hkv: int, D: int, L_cap: int,
-             dtype: int, mode: int, temperature: float = 1.0, shared_vocab: bool = False) -> Cfg:
+             dtype: int, mode: int, temperature: float = 1.0, shared_vocab: bool = False,
+             tree_nodes: Optional[Tuple[Sequence[int], Sequence[int]]] = None) -> Cfg:
+    """tree_nodes: (parent, rank) of a pruned tree's nodes in breadth-first rank-path order, or None
+    for the full Cartesian tree of ``branching``."""
     c = Cfg()
     c.B, c.d, c.V, c.K = B, d, V, len(branching)
     for i, s in enumerate(branching):
@@ -46,6 +50,11 @@ def make_cfg(B: int, d: int, V: int, branching: Sequence[int], Hq: int, Hkv: int
     c.Hq, c.Hkv, c.D, c.L_cap = Hq, Hkv, D, L_cap
     c.dtype, c.mode, c.temperature = dtype, mode, float(temperature)
     c.shared_vocab = 1 if shared_vocab else 0
+    if tree_nodes is not None:
+        parent, rank = tree_nodes
+        c.tree_nodes = len(parent)
+        for n, (p, r) in enumerate(zip(parent, rank)):
+            c.tree_parent[n], c.tree_rank[n] = int(p), int(r)
     return c
 
 

@@ -40,6 +40,7 @@ class Workload:
     compact: bool                     # KV compaction listed for the workload
     w_sigma: float = 0.02             # std of W_k and of the vocab projections
     shared_vocab: bool = False        # one vocab projection U for every head (U is [V][d])
+    tree_paths: Optional[Tuple[Tuple[int, ...], ...]] = None   # a pruned tree's non-root rank paths
     note: str = ""
 
     @property
@@ -48,12 +49,24 @@ class Workload:
 
     @property
     def N(self) -> int:
-        """Node count of the Cartesian tree: root plus every level."""
+        """Node count: the pruned tree's, or the Cartesian tree's (root plus every level)."""
+        if self.tree_paths is not None:
+            return 1 + len(self.tree_paths)
         n, cnt = 1, 1
         for s in self.branching:
             cnt *= s
             n += cnt
         return n
+
+    @property
+    def tree_nodes(self):
+        """(parent, rank) of every node of a pruned tree in breadth-first, rank-path
+        lexicographic order (node 0 = root), or None for the Cartesian tree."""
+        if self.tree_paths is None:
+            return None
+        order = [()] + sorted(self.tree_paths, key=lambda p: (len(p), p))
+        at = {p: n for n, p in enumerate(order)}
+        return [-1] + [at[p[:-1]] for p in order[1:]], [0] + [p[-1] for p in order[1:]]
 
     @property
     def s_max(self) -> int:
@@ -101,6 +114,35 @@ for _base in ("vicuna7b_b1", "vicuna13b_b8"):
         {k: getattr(_w, k) for k in _w.__dataclass_fields__}, name=_base + "_shared", shared_vocab=True,
         note=_w.note + "; every head projects with one shared (frozen LM-head) vocab matrix"))
 SHARED = ["vicuna7b_b1_shared", "vicuna13b_b8_shared"]
+
+
+def pruned_paths(K: int, s_max: int, count: int, decay: float = 0.5):
+    """The `count` rank paths of highest estimated reach in a depth-K tree whose
+    heads keep top-s_max lists, taking a candidate of rank r to be accepted with
+    probability proportional to decay**r (so a path's score is the product over
+    its ranks; prefixes always score higher, so the set is closed under prefixes).
+    Ties go to the shorter, then lexicographically smaller path."""
+    import heapq
+    heap, out = [(-1.0, 0, ())], []
+    while heap and len(out) < count + 1:
+        neg, _, p = heapq.heappop(heap)
+        out.append(p)
+        if len(p) < K:
+            for r in range(s_max):
+                q = p + (r,)
+                heapq.heappush(heap, (neg * decay ** r, len(q), q))
+    return tuple(sorted((p for p in out if p), key=lambda p: (len(p), p)))
+
+
+# Pruned 64-node trees (5 heads, top-8 lists) on the 7B and 13B step shapes.
+for _base in ("vicuna7b_b1", "vicuna13b_b8"):
+    _w = WORKLOADS[_base]
+    _paths = pruned_paths(5, 8, 63)
+    _br = tuple(1 + max(p[d] for p in _paths if len(p) > d) for d in range(5))
+    WORKLOADS[_base + "_pruned64"] = Workload(**dict(
+        {k: getattr(_w, k) for k in _w.__dataclass_fields__}, name=_base + "_pruned64", branching=_br,
+        tree_paths=_paths, note=_w.note.split(",")[0] + f", pruned 64-node tree over 5 heads (top-s {_br})"))
+PRUNED = ["vicuna7b_b1_pruned64", "vicuna13b_b8_pruned64"]
 
 
 def get(name: str) -> Workload:

@@ -28,10 +28,31 @@ int check_cfg(const medusa_cfg* c) {
     if (c->branching[k] > kMaxS || c->branching[k] > c->V) return MEDUSA_ERR_UNSUPPORTED;
   }
   long n = 1, cnt = 1;
-  for (int k = 0; k < c->K; ++k) {
-    cnt *= c->branching[k];
-    n += cnt;
-    if (n > kMaxN) return MEDUSA_ERR_UNSUPPORTED;
+  if (c->tree_nodes == 0) {
+    for (int k = 0; k < c->K; ++k) {
+      cnt *= c->branching[k];
+      n += cnt;
+      if (n > kMaxN) return MEDUSA_ERR_UNSUPPORTED;
+    }
+  } else {
+    // a pruned tree: breadth first, (parent, rank) increasing within a depth, ranks inside the top-s lists
+    if (c->tree_nodes < 1 || c->tree_nodes > kMaxN) return MEDUSA_ERR_UNSUPPORTED;
+    n = c->tree_nodes;
+    if (c->tree_parent[0] != -1) return MEDUSA_ERR_INVALID_ARG;
+    int depth[kMaxN];
+    depth[0] = 0;
+    for (int i = 1; i < n; ++i) {
+      const int p = c->tree_parent[i];
+      if (p < 0 || p >= i) return MEDUSA_ERR_INVALID_ARG;
+      depth[i] = depth[p] + 1;
+      if (depth[i] > c->K || c->tree_rank[i] >= c->branching[depth[i] - 1]) return MEDUSA_ERR_INVALID_ARG;
+      if (i > 1) {
+        const int q = c->tree_parent[i - 1];
+        if (depth[i] < depth[i - 1] || depth[i] > depth[i - 1] + 1) return MEDUSA_ERR_INVALID_ARG;
+        if (depth[i] == depth[i - 1] && !(p > q || (p == q && c->tree_rank[i] > c->tree_rank[i - 1])))
+          return MEDUSA_ERR_INVALID_ARG;
+      }
+    }
   }
   if (c->Hq % c->Hkv != 0) return MEDUSA_ERR_UNSUPPORTED;
   if (c->D != 64 && c->D != 128) return MEDUSA_ERR_UNSUPPORTED;
@@ -111,7 +132,8 @@ int medusa_verify(const medusa_cfg* cfg, const int32_t* tokens, const int32_t* p
                   void* workspace, medusa_stream_t stream) {
   int s = check_cfg(cfg);
   if (s != MEDUSA_OK) return s;
-  if (!tokens || !first_child || !target_logits || !acc || !path || !out_tokens || !n_out || !flags || !workspace)
+  if (!tokens || !parent || !first_child || !target_logits || !acc || !path || !out_tokens || !n_out || !flags ||
+      !workspace)
     return MEDUSA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MEDUSA_ERR_INVALID_ARG;
   char* ws = static_cast<char*>(workspace) + align_up(heads_workspace(*cfg), 256) +

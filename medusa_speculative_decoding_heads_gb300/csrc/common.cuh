@@ -43,7 +43,8 @@ struct TreeShape {
   int s_max;
   int s[kMaxK + 1];     // s[1..K]
   int cnt[kMaxK + 1];   // cnt[d] = prod_{j<=d} s_j, cnt[0] = 1
-  int off[kMaxK + 2];   // off[d] = sum_{e<d} cnt[e]; off[K+1] = N
+  int off[kMaxK + 2];   // off[d] = sum_{e<d} cnt[e]; off[K+1] = N (Cartesian tree)
+  int pruned;           // 1: N comes from a pruned tree's node list (cnt/off unused)
 };
 
 inline TreeShape tree_shape(const medusa_cfg& c) {
@@ -59,6 +60,10 @@ inline TreeShape tree_shape(const medusa_cfg& c) {
   }
   for (int d = 1; d <= c.K + 1; ++d) t.off[d] = t.off[d - 1] + t.cnt[d - 1];
   t.N = t.off[c.K + 1];
+  if (c.tree_nodes > 0) {   // a pruned tree: its own node count
+    t.N = c.tree_nodes;
+    t.pruned = 1;
+  }
   return t;
 }
 

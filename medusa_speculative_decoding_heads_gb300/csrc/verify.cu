@@ -320,8 +320,8 @@ __device__ __forceinline__ int row_best(const int2* __restrict__ pr, int P) {
 
 // Greedy walk from the per-row argmax. One thread per sequence.
 __global__ void greedy_walk_kernel(TreeShape ts, int B, const int32_t* __restrict__ tokens,
-                                   const int32_t* __restrict__ first_child, const int2* __restrict__ part, int P,
-                                   WalkOut w) {
+                                   const int32_t* __restrict__ parent, const int32_t* __restrict__ first_child,
+                                   const int2* __restrict__ part, int P, WalkOut w) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
@@ -336,7 +336,7 @@ __global__ void greedy_walk_kernel(TreeShape ts, int B, const int32_t* __restric
     const int a = row_best(part + ((size_t)b * N + cur) * P, P);
     const int fc = first_child[cur];
     int nx = -1;
-    for (int j = 0; j < ts.s[dep] && fc >= 0 && fc + j < N; ++j)
+    for (int j = 0; fc >= 0 && fc + j < N && parent[fc + j] == cur; ++j)   // cur's children
       if (tok[fc + j] == a) nx = fc + j;
     if (nx < 0) break;
     out[acc] = a;
@@ -738,7 +738,8 @@ __device__ int walk_inverse_cdf(const float (&pc)[C], int lo, int hi, int V, flo
 template <typename T, int C, bool VEC>
 __global__ void __launch_bounds__(kVThreads, 1)
 rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restrict__ tokens,
-               const int32_t* __restrict__ first_child, const T* __restrict__ tl, const float* __restrict__ hl,
+               const int32_t* __restrict__ parent, const int32_t* __restrict__ first_child,
+               const T* __restrict__ tl, const float* __restrict__ hl,
                const float2* __restrict__ hstats, int hsP, const float* __restrict__ u_acc,
                const float* __restrict__ u_res, WalkOut w) {
   pdl_wait();
@@ -753,10 +754,11 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
   const int lo = min(V, (int)rank * slice), hi = min(V, lo + slice);
   const float c = 1.4426950408889634f / Tmp;
   // this sequence's tree tokens and the tree's first-child table, staged once
-  __shared__ int s_tok[kMaxN], s_fc[kMaxN];
+  __shared__ int s_tok[kMaxN], s_fc[kMaxN], s_par[kMaxN];
   for (int i = threadIdx.x; i < N; i += kVThreads) {
     s_tok[i] = tokens[(size_t)b * N + i];
     s_fc[i] = first_child[i];
+    s_par[i] = parent[i];
   }
   uint32_t fl = 0;
   int xn = 0;
@@ -784,7 +786,7 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
     if (fetch) {
       const int fc = s_fc[cur];
       const int j = threadIdx.x;
-      const int xt = (fc >= 0 && fc + j < N) ? min(max(s_tok[fc + j], 0), V - 1) : 0;
+      const int xt = (fc >= 0 && fc + j < N && s_par[fc + j] == cur) ? min(max(s_tok[fc + j], 0), V - 1) : 0;
       ct = Elt<T>::load(trow, xt);
       ch = hl[((size_t)b * K + (dep - 1)) * V + xt];
       cu = u_acc[((size_t)b * K + (dep - 1)) * ts.s_max + j];
@@ -799,7 +801,7 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
       const int lines = ((hi - lo) * (int)sizeof(T) + 127) / 128;   // every prefetched line starts inside the slice
       for (int t = threadIdx.x; t < ts.s[dep] * lines; t += kVThreads) {
         const int j = t / lines, l = t % lines;
-        if (fc >= 0 && fc + j < N) {
+        if (fc >= 0 && fc + j < N && s_par[fc + j] == cur) {
           const char* pr = reinterpret_cast<const char*>(tl + ((size_t)b * N + fc + j) * V + lo) + 128 * l;
           asm volatile("prefetch.global.L2 [%0];" ::"l"(pr));
         }
@@ -822,7 +824,7 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
       cand_u[j] = cu;
       if (j == 0) {
         int nc = 0;
-        while (nc < ts.s[dep] && fc >= 0 && fc + nc < N) ++nc;
+        while (nc < ts.s[dep] && fc >= 0 && fc + nc < N && s_par[fc + nc] == cur) ++nc;   // cur's children
         cand_n = nc;
         cand_q = merge_head_stats(hq, c);
       }
@@ -917,7 +919,7 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
 
 template <typename T, int C, bool VEC>
 cudaError_t launch_rs_walk_v(const medusa_cfg& c, const TreeShape& ts, int ncta, int slice, const int32_t* tokens,
-                             const int32_t* first_child, const void* tl, const float* hl, const float2* stats, int hsP,
+                             const int32_t* parent, const int32_t* first_child, const void* tl, const float* hl, const float2* stats, int hsP,
                              const float* ua, const float* ur, const WalkOut& w, cudaStream_t st) {
   const size_t smem = (size_t)C * kPad * sizeof(float);
   auto kern = rs_walk_kernel<T, C, VEC>;
@@ -937,8 +939,8 @@ cudaError_t launch_rs_walk_v(const medusa_cfg& c, const TreeShape& ts, int ncta,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, kern, ts, c.V, slice, c.temperature, tokens, first_child, static_cast<const T*>(tl), hl,
-                         stats, hsP, ua, ur, w);
+  e = cudaLaunchKernelEx(&cfg, kern, ts, c.V, slice, c.temperature, tokens, parent, first_child,
+                         static_cast<const T*>(tl), hl, stats, hsP, ua, ur, w);
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -947,11 +949,11 @@ cudaError_t launch_rs_walk_v(const medusa_cfg& c, const TreeShape& ts, int ncta,
 // Vector loads need V % 8 == 0 (aligned rows and slices) and at least 8 entries per thread.
 template <typename T, int C>
 cudaError_t launch_rs_walk(const medusa_cfg& c, const TreeShape& ts, int ncta, int slice, const int32_t* tokens,
-                           const int32_t* first_child, const void* tl, const float* hl, const float2* stats, int hsP,
+                           const int32_t* parent, const int32_t* first_child, const void* tl, const float* hl, const float2* stats, int hsP,
                            const float* ua, const float* ur, const WalkOut& w, cudaStream_t st) {
   if (C >= 8 && c.V % 8 == 0)
-    return launch_rs_walk_v<T, C, (C >= 8)>(c, ts, ncta, slice, tokens, first_child, tl, hl, stats, hsP, ua, ur, w, st);
-  return launch_rs_walk_v<T, C, false>(c, ts, ncta, slice, tokens, first_child, tl, hl, stats, hsP, ua, ur, w, st);
+    return launch_rs_walk_v<T, C, (C >= 8)>(c, ts, ncta, slice, tokens, parent, first_child, tl, hl, stats, hsP, ua, ur, w, st);
+  return launch_rs_walk_v<T, C, false>(c, ts, ncta, slice, tokens, parent, first_child, tl, hl, stats, hsP, ua, ur, w, st);
 }
 
 // CTAs per sequence: the largest power of two (at most 8) that keeps the whole
@@ -963,7 +965,8 @@ int rs_cluster_ctas(int B) {
 }
 
 template <typename T>
-cudaError_t run_rs(const medusa_cfg& c, const TreeShape& ts, const int32_t* tokens, const int32_t* first_child,
+cudaError_t run_rs(const medusa_cfg& c, const TreeShape& ts, const int32_t* tokens, const int32_t* parent,
+                   const int32_t* first_child,
                    const void* tl, const float* hl, const float* ua, const float* ur, const WalkOut& w, float2* stats,
                    cudaStream_t st) {
   const float cs = 1.4426950408889634f / c.temperature;
@@ -979,7 +982,7 @@ cudaError_t run_rs(const medusa_cfg& c, const TreeShape& ts, const int32_t* toke
   const int ncta = rs_cluster_ctas(c.B);
   const int slice = (((c.V + ncta - 1) / ncta) + 7) / 8 * 8;
   const int need = (slice + kVThreads - 1) / kVThreads;
-#define MEDUSA_RS(CC) return launch_rs_walk<T, CC>(c, ts, ncta, slice, tokens, first_child, tl, hl, stats, hsP, ua, ur, w, st)
+#define MEDUSA_RS(CC) return launch_rs_walk<T, CC>(c, ts, ncta, slice, tokens, parent, first_child, tl, hl, stats, hsP, ua, ur, w, st)
   if (need <= 1) MEDUSA_RS(1);
   if (need <= 2) MEDUSA_RS(2);
   if (need <= 4) MEDUSA_RS(4);
@@ -990,7 +993,8 @@ cudaError_t run_rs(const medusa_cfg& c, const TreeShape& ts, const int32_t* toke
 }
 
 template <typename T>
-cudaError_t run_greedy(const medusa_cfg& c, const TreeShape& ts, const int32_t* tokens, const int32_t* first_child,
+cudaError_t run_greedy(const medusa_cfg& c, const TreeShape& ts, const int32_t* tokens, const int32_t* parent,
+                       const int32_t* first_child,
                        const void* tl, const WalkOut& w, int2* part, cudaStream_t st) {
   const int P = row_slices((long)c.B * ts.N, c.V, kMaxRowSlices);
   const int chunk = slice_len(c.V, P);
@@ -1003,7 +1007,7 @@ cudaError_t run_greedy(const medusa_cfg& c, const TreeShape& ts, const int32_t* 
   note_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  launch_pdl(greedy_walk_kernel, (c.B + 127) / 128, 128, 0, st, ts, c.B, tokens, first_child, part, P, w);
+  launch_pdl(greedy_walk_kernel, (c.B + 127) / 128, 128, 0, st, ts, c.B, tokens, parent, first_child, part, P, w);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -1021,17 +1025,16 @@ cudaError_t launch_verify(const medusa_cfg& c, const int32_t* tokens, const int3
                           const void* tl, const float* hl, const float* u_acc, const float* u_res, int32_t* acc,
                           int32_t* path, int32_t* out_tokens, int32_t* n_out, uint32_t* flags, void* ws,
                           cudaStream_t st) {
-  (void)parent;
   const TreeShape ts = tree_shape(c);
   WalkOut w{acc, path, out_tokens, n_out, flags};
   if (c.mode == MEDUSA_GREEDY) {
     int2* part = static_cast<int2*>(ws);
-    return c.dtype == MEDUSA_F32 ? run_greedy<float>(c, ts, tokens, first_child, tl, w, part, st)
-                                 : run_greedy<uint16_t>(c, ts, tokens, first_child, tl, w, part, st);
+    return c.dtype == MEDUSA_F32 ? run_greedy<float>(c, ts, tokens, parent, first_child, tl, w, part, st)
+                                 : run_greedy<uint16_t>(c, ts, tokens, parent, first_child, tl, w, part, st);
   }
   float2* stats = static_cast<float2*>(ws);
-  return c.dtype == MEDUSA_F32 ? run_rs<float>(c, ts, tokens, first_child, tl, hl, u_acc, u_res, w, stats, st)
-                               : run_rs<uint16_t>(c, ts, tokens, first_child, tl, hl, u_acc, u_res, w, stats, st);
+  return c.dtype == MEDUSA_F32 ? run_rs<float>(c, ts, tokens, parent, first_child, tl, hl, u_acc, u_res, w, stats, st)
+                               : run_rs<uint16_t>(c, ts, tokens, parent, first_child, tl, hl, u_acc, u_res, w, stats, st);
 }
 
 }  // namespace medusa

@@ -21,7 +21,8 @@ from .configs import F32, GREEDY, REJECTION, Workload
 def cfg_for(w: Workload, L_cap: int, mode: int, B: Optional[int] = None) -> mb.Cfg:
     return mb.make_cfg(B=w.B if B is None else B, d=w.d, V=w.V, branching=w.branching, Hq=w.Hq, Hkv=w.Hkv,
                        D=w.D, L_cap=L_cap, dtype=w.dtype, mode=mode,
-                       temperature=w.temperature if mode == REJECTION else 1.0, shared_vocab=w.shared_vocab)
+                       temperature=w.temperature if mode == REJECTION else 1.0, shared_vocab=w.shared_vocab,
+                       tree_nodes=w.tree_nodes)
 
 
 class DeviceStep:

@@ -54,8 +54,9 @@ def random_topk(rng, B, K, s_max, branching, V):
 def planted_greedy_logits(logits: torch.Tensor, tree: dict, seed: int, K: int):
     """Boost a seeded random path so the greedy walk accepts a seeded number of drafts.
 
-    For sequence b a depth a in 0..K and a path of a nodes are drawn; the target
-    logit of each path node's token is raised at its parent. Returns the depths.
+    For sequence b a depth a in 0..K and a path of a nodes are drawn (shorter if
+    it reaches a leaf of a pruned tree first); the target logit of each path
+    node's token is raised at its parent. Returns the planted depths.
     """
     rng = np.random.default_rng(seed)
     B = logits.shape[0]
@@ -64,8 +65,11 @@ def planted_greedy_logits(logits: torch.Tensor, tree: dict, seed: int, K: int):
         a = int(rng.integers(0, K + 1))
         cur = 0
         nodes, toks = [], []
-        for _ in range(a):
+        for step in range(a):
             kids = O.children_of(tree["parent"], cur)
+            if not kids:
+                a = step
+                break
             nxt = kids[int(rng.integers(len(kids)))]
             nodes.append(cur)
             toks.append(int(tree["tokens"][b, nxt]))

@@ -100,3 +100,36 @@ def test_rejection_mode_needs_logits_and_uniforms(lib):
     assert lib.medusa_heads(ctypes.byref(cfg), fake, fake, None, fake, None, fake, fake, None) == -1
     assert lib.medusa_verify(ctypes.byref(cfg), fake, fake, fake, fake, None, None, None, fake, fake, fake, fake,
                              fake, fake, None) == -1
+
+
+def test_pruned_and_shared_configs(lib):
+    """The extra workloads (one shared vocab projection, pruned 64-node trees) pass
+    the checks and report their own node counts."""
+    for name in configs.SHARED + configs.PRUNED:
+        w = configs.get(name)
+        cfg = cfg_for(w, L_cap=w.L_range[1] + w.N, mode=w.modes[0])
+        assert mb.node_count(cfg) == w.N
+        assert mb.workspace_size(cfg) > 0
+    assert configs.get("vicuna7b_b1_pruned64").N == 64
+
+
+@pytest.mark.parametrize("edit", ["root_parent", "forward_parent", "rank_too_big", "too_deep", "sibling_order",
+                                  "depth_order"])
+def test_malformed_pruned_trees_are_rejected(lib, edit):
+    w = configs.get("vicuna7b_b1_pruned64")
+    parent, rank = (list(x) for x in w.tree_nodes)
+    if edit == "root_parent":
+        parent[0] = 0
+    elif edit == "forward_parent":
+        parent[5] = 7
+    elif edit == "rank_too_big":
+        rank[1] = w.branching[0]
+    elif edit == "too_deep":
+        w = configs.scaled(w, branching=w.branching[:4])   # the tree has depth-5 nodes
+    elif edit == "sibling_order":
+        rank[1], rank[2] = rank[2], rank[1]
+    elif edit == "depth_order":
+        parent[6] = 5          # node 6 drops to depth 3 while node 7 stays at depth 2: not breadth first
+    cfg = mb.make_cfg(B=w.B, d=w.d, V=w.V, branching=w.branching, Hq=w.Hq, Hkv=w.Hkv, D=w.D, L_cap=4096,
+                      dtype=w.dtype, mode=configs.GREEDY, tree_nodes=(parent, rank))
+    assert mb.raw_call("medusa_workspace_size", ctypes.byref(cfg), ctypes.byref(ctypes.c_size_t())) == -1

@@ -30,12 +30,17 @@ def small(w):
     return configs.scaled(w, d=512, V=1000, Hq=2 * G, Hkv=2, L_range=(37, 300))
 
 
+def layout(w):
+    """The oracle's layout of the workload's tree (pruned or Cartesian)."""
+    return O.tree_layout(w.branching) if w.tree_paths is None else O.tree_layout_from_paths(w.tree_paths, w.branching)
+
+
 def oracle_tree(w, root, topk, L, L_cap):
-    return O.tree_build(w.branching, np.asarray(root), np.asarray(topk), np.asarray(L), L_cap)
+    return O.tree_build(w.branching, np.asarray(root), np.asarray(topk), np.asarray(L), L_cap, paths=w.tree_paths)
 
 
 # --------------------------------------------------------------------------- tree build
-@pytest.mark.parametrize("name", NAMES)
+@pytest.mark.parametrize("name", NAMES + configs.PRUNED)
 def test_tree_build_bit_exact(name):
     dev = gpu_ready()
     w = configs.get(name)
@@ -181,7 +186,7 @@ def test_heads_topk_ties(name, groups):
 
 # --------------------------------------------------------------------------- attention
 def check_attention(w, si, O_gpu, pairs):
-    tree = O.tree_layout(w.branching)
+    tree = layout(w)
     mask = O.ancestor_mask(tree["parent"])
     G = w.Hq // w.Hkv
     worst = 0.0
@@ -205,7 +210,7 @@ def run_attention(w, si, dev):
     return st
 
 
-@pytest.mark.parametrize("name", NAMES)
+@pytest.mark.parametrize("name", NAMES + configs.PRUNED)
 def test_attention_small_all_heads(name):
     dev = gpu_ready()
     w = small(configs.get(name))
@@ -264,7 +269,7 @@ def greedy_case(w, dev, seed):
     return L, L_cap, root, topk, tree, tl, depths
 
 
-@pytest.mark.parametrize("name", NAMES)
+@pytest.mark.parametrize("name", NAMES + configs.PRUNED)
 def test_verify_greedy_bit_exact(name):
     dev = gpu_ready()
     w = configs.scaled(configs.get(name), B=max(configs.get(name).B, 12), target_corr=0.0)
@@ -325,7 +330,8 @@ def rs_case(w, dev, seed, sigma_head=2.0):
 
 
 @pytest.mark.parametrize("name,T", [("tiny_fp32", 1.0), ("vicuna13b_b8", 1.0), ("gqa7b_b32", 0.7),
-                                    ("vicuna7b_b1", 0.5), ("vicuna33b_b16", 1.3)])
+                                    ("vicuna7b_b1", 0.5), ("vicuna33b_b16", 1.3),
+                                    ("vicuna13b_b8_pruned64", 1.0), ("vicuna7b_b1_pruned64", 0.7)])
 def test_verify_rejection_decisions(name, T):
     dev = gpu_ready()
     w = configs.scaled(configs.get(name), temperature=T)
@@ -383,7 +389,7 @@ def test_kv_compact_bit_exact(name):
     w = small(configs.get(name))
     si = synth.make_step_inputs(w, seed=9, device=dev)
     rng = np.random.default_rng(9)
-    tree = O.tree_layout(w.branching)
+    tree = layout(w)
     acc = rng.integers(0, w.K + 1, size=w.B).astype(np.int32)
     acc[0] = 0
     acc[-1] = w.K
@@ -410,7 +416,7 @@ def test_kv_compact_bit_exact(name):
 
 
 # --------------------------------------------------------------------------- whole step
-@pytest.mark.parametrize("name", NAMES + configs.SHARED)
+@pytest.mark.parametrize("name", NAMES + configs.SHARED + configs.PRUNED)
 def test_step_end_to_end_small(name):
     """The five calls in order on one stream against the oracle's step on the same inputs."""
     dev = gpu_ready()
