@@ -476,6 +476,65 @@ def kv_compact(Kc: np.ndarray, Vc: np.ndarray, L: np.ndarray, acc: np.ndarray, p
     return Kc, Vc, L_new, kv_map
 
 
+# --------------------------------------------------------------------------- paged cache (NEXT f4)
+def paged_rows(pool: np.ndarray, block_table: np.ndarray, b: int, rows: int, page_rows: int) -> np.ndarray:
+    """Logical rows [0, rows) of sequence b from a paged pool, [Hkv][rows][D].
+
+    R15: a paged cache is a storage layout of the same logical cache: logical
+    row i of sequence b lives in page block_table[b][i // P] at offset i % P,
+    pool [num_pages][Hkv][P][D] (P = page_rows).
+    """
+    idx = np.arange(rows)
+    pages = block_table[b, idx // page_rows]
+    return pool[pages, :, idx % page_rows, :].transpose(1, 0, 2)
+
+
+def tree_attention_paged(Q, Kp, Vp, block_table, page_rows, Kt, Vt, L, mask, Hq, Hkv, pairs=None):
+    """Tree attention with the committed prefix in a paged pool and the tree's
+    own keys/values in a staging buffer Kt, Vt [B][Hkv][N][D] (R15): the
+    logical cache of each sequence is its paged prefix followed by its tree
+    rows, and the result is tree_attention over that cache."""
+    B, N = Q.shape[0], Q.shape[1]
+    Hkv_, D = Kt.shape[1], Kt.shape[3]
+    cap = int(np.max(L)) + N
+    Kc = np.zeros((B, Hkv_, cap, D))
+    Vc = np.zeros((B, Hkv_, cap, D))
+    for b in range(B):
+        Lb = int(L[b])
+        Kc[b, :, :Lb] = paged_rows(Kp, block_table, b, Lb, page_rows)
+        Vc[b, :, :Lb] = paged_rows(Vp, block_table, b, Lb, page_rows)
+        Kc[b, :, Lb:Lb + N] = Kt[b]
+        Vc[b, :, Lb:Lb + N] = Vt[b]
+    return tree_attention(Q, Kc, Vc, L, mask, Hq, Hkv, pairs)
+
+
+def kv_commit_paged(Kp_layers, Vp_layers, block_table, page_rows, Kt_layers, Vt_layers, L, acc, path):
+    """Keep the accepted path in a paged cache, in every layer (R15, R11).
+
+    For each layer and sequence b: logical row L_b + r (r = 0..acc_b) receives
+    the tree row path[b][r] of that layer's staging buffer; then L_b grows by
+    acc_b + 1. This is R11's compaction of the logical cache whose rows
+    L_b .. L_b + N - 1 hold the tree. Returns new pools (one per layer), L and
+    kv_map.
+    """
+    Kp_layers = [k.copy() for k in Kp_layers]
+    Vp_layers = [v.copy() for v in Vp_layers]
+    B, K1 = path.shape
+    L_new = L.astype(np.int64).copy()
+    kv_map = np.full((B, K1), -1, dtype=np.int64)
+    for b in range(B):
+        Lb, n = int(L[b]), int(acc[b]) + 1
+        for r in range(n):
+            row = Lb + r
+            page, off = int(block_table[b, row // page_rows]), row % page_rows
+            for Kp, Vp, Kt, Vt in zip(Kp_layers, Vp_layers, Kt_layers, Vt_layers):
+                Kp[page, :, off, :] = Kt[b, :, int(path[b, r]), :]
+                Vp[page, :, off, :] = Vt[b, :, int(path[b, r]), :]
+        kv_map[b, :n] = path[b, :n]
+        L_new[b] = Lb + n
+    return Kp_layers, Vp_layers, L_new, kv_map
+
+
 # --------------------------------------------------------------------------- helpers
 def _pad(xs: Sequence[int], n: int) -> np.ndarray:
     out = np.full(n, -1, dtype=np.int64)
