@@ -207,6 +207,36 @@ MEDUSA_API int medusa_verify(const medusa_cfg* cfg, const int32_t* tokens, const
 MEDUSA_API int medusa_kv_compact(const medusa_cfg* cfg, void* Kc, void* Vc, int32_t* L, const int32_t* acc,
                       const int32_t* path, int32_t* kv_map, medusa_stream_t stream);
 
+/* Tree attention over a paged KV cache (R15 of the design
+ * notes: a page pool is a storage layout of the same logical cache).
+ *   Kp, Vp [num_pages][Hkv][page_rows][D] bf16  page pool of the committed rows
+ *   block_table [B][L_cap / page_rows] int32   logical rows [i P, (i+1) P) of
+ *                                               sequence b live in page
+ *                                               block_table[b][i] (P = page_rows)
+ *   Kt, Vt [B][Hkv][N][D] bf16                  the tree nodes' keys and values,
+ *                                               staged outside the cache
+ *   Q, L, anc_bits, O, workspace                as for medusa_tree_attention
+ * Every node attends to the logical rows [0, L_b) and to its ancestors-or-self
+ * among the staged rows. page_rows must be a positive multiple of 128 dividing
+ * cfg->L_cap; bf16 with D = 128 only (MEDUSA_ERR_UNSUPPORTED otherwise). */
+MEDUSA_API int medusa_tree_attention_paged(const medusa_cfg* cfg, const void* Q, const void* Kp, const void* Vp,
+                                int32_t num_pages, int32_t page_rows, const int32_t* block_table,
+                                const void* Kt, const void* Vt, const int32_t* L, const uint64_t* anc_bits,
+                                void* O, void* workspace, medusa_stream_t stream);
+
+/* Commit the accepted path into a paged cache, in every layer (NEXT f4).
+ * For layer l < n_layers the pools are Kp + l * pool_layer_elems (elements of
+ * the cfg's type; same for Vp) and the staged rows Kt + l * tree_layer_elems:
+ * for r = 0..acc_b, logical row L_b + r of sequence b receives the staged row
+ * path[b][r] in every KV head; then L_b += acc_b + 1 (in/out) and kv_map as for
+ * medusa_kv_compact. Sequences with L_b < 0 or L_b + N > L_cap are left as they
+ * are (kv_map = -1). Layouts and page_rows as for medusa_tree_attention_paged
+ * (any dtype and D). */
+MEDUSA_API int medusa_kv_commit_paged(const medusa_cfg* cfg, void* Kp, void* Vp, int32_t page_rows,
+                           const int32_t* block_table, const void* Kt, const void* Vt, int32_t n_layers,
+                           size_t pool_layer_elems, size_t tree_layer_elems, int32_t* L, const int32_t* acc,
+                           const int32_t* path, int32_t* kv_map, medusa_stream_t stream);
+
 /* Tree attention for callers that cannot allocate device memory.
  * No counterpart on the source pages: this is a deployment variant of
  * medusa_tree_attention for callers that cannot call cudaMalloc (for example a

@@ -21,7 +21,8 @@ FLAG_RS_NEAR_TIE, FLAG_CDF_NEAR_TIE, FLAG_CAPACITY = 1, 2, 4
 
 ENTRY_POINTS = ("medusa_node_count", "medusa_workspace_size", "medusa_heads", "medusa_tree_build",
                 "medusa_tree_attention", "medusa_verify", "medusa_kv_compact", "medusa_tree_attention_noalloc",
-                "medusa_launch_count", "medusa_status_string")
+                "medusa_tree_attention_paged", "medusa_kv_commit_paged", "medusa_launch_count",
+                "medusa_status_string")
 
 
 class MedusaError(RuntimeError):
@@ -78,6 +79,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "medusa_tree_build": [cp, P, P, P, P, P, P, P, P, P, P, P, P],
         "medusa_tree_attention": [cp, P, P, P, P, P, P, P, P],
         "medusa_tree_attention_noalloc": [cp, P, P, P, P, P, P, P],
+        "medusa_tree_attention_paged": [cp, P, P, P, ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P, P, P],
+        "medusa_kv_commit_paged": [cp, P, P, ctypes.c_int32, P, P, P, ctypes.c_int32, ctypes.c_size_t,
+                                   ctypes.c_size_t, P, P, P, P, P],
         "medusa_verify": [cp, P, P, P, P, P, P, P, P, P, P, P, P, P, P],
         "medusa_kv_compact": [cp, P, P, P, P, P, P, P],
     }
@@ -152,6 +156,22 @@ def tree_attention(cfg, Q, Kc, Vc, L, anc_bits, O, workspace, stream=None):
     _check("medusa_tree_attention", load().medusa_tree_attention(
         ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), _ptr(L), _ptr(anc_bits), _ptr(O), _ptr(workspace),
         _stream(stream)))
+
+
+def tree_attention_paged(cfg, Q, Kp, Vp, num_pages, page_rows, block_table, Kt, Vt, L, anc_bits, O, workspace,
+                         stream=None):
+    """medusa_tree_attention over a paged pool, the tree's rows staged in Kt/Vt."""
+    _check("medusa_tree_attention_paged", load().medusa_tree_attention_paged(
+        ctypes.byref(cfg), _ptr(Q), _ptr(Kp), _ptr(Vp), int(num_pages), int(page_rows), _ptr(block_table), _ptr(Kt),
+        _ptr(Vt), _ptr(L), _ptr(anc_bits), _ptr(O), _ptr(workspace), _stream(stream)))
+
+
+def kv_commit_paged(cfg, Kp, Vp, page_rows, block_table, Kt, Vt, n_layers, pool_layer_elems, tree_layer_elems, L, acc,
+                    path, kv_map, stream=None):
+    """Write the accepted path's staged rows into the paged pools of n_layers layers."""
+    _check("medusa_kv_commit_paged", load().medusa_kv_commit_paged(
+        ctypes.byref(cfg), _ptr(Kp), _ptr(Vp), int(page_rows), _ptr(block_table), _ptr(Kt), _ptr(Vt), int(n_layers),
+        int(pool_layer_elems), int(tree_layer_elems), _ptr(L), _ptr(acc), _ptr(path), _ptr(kv_map), _stream(stream)))
 
 
 def tree_attention_noalloc(cfg, Q, Kc, Vc, L, anc_bits, O, stream=None):

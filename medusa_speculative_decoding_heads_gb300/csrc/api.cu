@@ -155,6 +155,42 @@ int medusa_kv_compact(const medusa_cfg* cfg, void* Kc, void* Vc, int32_t* L, con
   return from_cuda(launch_kv_compact(*cfg, Kc, Vc, L, acc, path, kv_map, (cudaStream_t)stream));
 }
 
+int medusa_tree_attention_paged(const medusa_cfg* cfg, const void* Q, const void* Kp, const void* Vp, int32_t num_pages,
+                                int32_t page_rows, const int32_t* block_table, const void* Kt, const void* Vt,
+                                const int32_t* L, const uint64_t* anc_bits, void* O, void* workspace,
+                                medusa_stream_t stream) {
+  int s = check_cfg(cfg);
+  if (s != MEDUSA_OK) return s;
+  if (!Q || !Kp || !Vp || !block_table || !Kt || !Vt || !L || !anc_bits || !O || !workspace || num_pages < 1)
+    return MEDUSA_ERR_INVALID_ARG;
+  if (page_rows < 128 || page_rows % 128 != 0 || cfg->L_cap % page_rows != 0) return MEDUSA_ERR_UNSUPPORTED;
+  if (cfg->dtype != MEDUSA_BF16 || cfg->D != 128) return MEDUSA_ERR_UNSUPPORTED;
+  if (!aligned16(Q) || !aligned16(Kp) || !aligned16(Vp) || !aligned16(Kt) || !aligned16(Vt) || !aligned16(O))
+    return MEDUSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MEDUSA_ERR_INVALID_ARG;
+  char* ws = static_cast<char*>(workspace) + align_up(heads_workspace(*cfg), 256);
+  const PagedKV pg{num_pages, page_rows, block_table, Kt, Vt};
+  return from_cuda(launch_attention(*cfg, Q, Kp, Vp, L, anc_bits, O, ws, (cudaStream_t)stream, &pg));
+}
+
+int medusa_kv_commit_paged(const medusa_cfg* cfg, void* Kp, void* Vp, int32_t page_rows, const int32_t* block_table,
+                           const void* Kt, const void* Vt, int32_t n_layers, size_t pool_layer_elems,
+                           size_t tree_layer_elems, int32_t* L, const int32_t* acc, const int32_t* path,
+                           int32_t* kv_map, medusa_stream_t stream) {
+  int s = check_cfg(cfg);
+  if (s != MEDUSA_OK) return s;
+  if (!Kp || !Vp || !block_table || !Kt || !Vt || !L || !acc || !path || !kv_map || n_layers < 1)
+    return MEDUSA_ERR_INVALID_ARG;
+  if (page_rows < 128 || page_rows % 128 != 0 || cfg->L_cap % page_rows != 0) return MEDUSA_ERR_UNSUPPORTED;
+  const size_t per16 = cfg->dtype == MEDUSA_F32 ? 4 : 8;
+  if (!aligned16(Kp) || !aligned16(Vp) || !aligned16(Kt) || !aligned16(Vt) || pool_layer_elems % per16 != 0 ||
+      tree_layer_elems % per16 != 0 || (n_layers > 1 && (pool_layer_elems == 0 || tree_layer_elems == 0)))
+    return MEDUSA_ERR_INVALID_ARG;
+  const PagedKV pg{0, page_rows, block_table, Kt, Vt};
+  return from_cuda(launch_kv_commit_paged(*cfg, Kp, Vp, pg, n_layers, pool_layer_elems, tree_layer_elems, L, acc, path,
+                                          kv_map, (cudaStream_t)stream));
+}
+
 uint64_t medusa_launch_count(void) { return (uint64_t)g_launches.load(std::memory_order_relaxed); }
 
 const char* medusa_status_string(int status) {

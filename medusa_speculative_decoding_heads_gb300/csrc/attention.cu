@@ -237,14 +237,14 @@ __global__ void tree_attn_merge_kernel(const float* __restrict__ o_part, const f
 
 template <typename T, int D>
 cudaError_t run(const medusa_cfg& c, const AttnPlan& p, const void* Q, const void* Kc, const void* Vc,
-                const int32_t* L, const uint64_t* bits, void* O, char* ws, cudaStream_t st) {
+                const int32_t* L, const uint64_t* bits, void* O, char* ws, cudaStream_t st, const PagedKV* paged) {
   const TreeShape ts = tree_shape(c);
   float* o_part = reinterpret_cast<float*>(ws + p.o_part);
   float* ml_part = reinterpret_cast<float*>(ws + p.ml_part);
   cudaError_t e;
   const int path = attention_path(c);
   if (path == kPathTc) {
-    e = launch_attention_tc(c, p.nsplit, p.chunk, Q, Kc, Vc, L, bits, o_part, ml_part, O, st);
+    e = launch_attention_tc(c, p.nsplit, p.chunk, Q, Kc, Vc, L, bits, o_part, ml_part, O, st, paged);
     if (e != cudaSuccess || p.nsplit == 1) return e;   // a single split writes O itself
   } else if (path == kPathMma) {
     e = launch_attention_mma(c, p.nsplit, p.chunk, Q, Kc, Vc, L, bits, o_part, ml_part, st);
@@ -270,15 +270,16 @@ cudaError_t run(const medusa_cfg& c, const AttnPlan& p, const void* Q, const voi
 size_t attention_workspace(const medusa_cfg& c) { return plan_attention(c).total; }
 
 cudaError_t launch_attention(const medusa_cfg& c, const void* Q, const void* Kc, const void* Vc, const int32_t* L,
-                             const uint64_t* bits, void* O, void* ws, cudaStream_t st) {
+                             const uint64_t* bits, void* O, void* ws, cudaStream_t st, const PagedKV* paged) {
   const AttnPlan p = plan_attention(c);
   char* w = static_cast<char*>(ws);
+  if (paged && attention_path(c) != kPathTc) return cudaErrorNotSupported;   // paged: the tcgen05 kernel only
   if (c.dtype == MEDUSA_F32) {
-    return c.D == 64 ? run<float, 64>(c, p, Q, Kc, Vc, L, bits, O, w, st)
-                     : run<float, 128>(c, p, Q, Kc, Vc, L, bits, O, w, st);
+    return c.D == 64 ? run<float, 64>(c, p, Q, Kc, Vc, L, bits, O, w, st, paged)
+                     : run<float, 128>(c, p, Q, Kc, Vc, L, bits, O, w, st, paged);
   }
-  return c.D == 64 ? run<uint16_t, 64>(c, p, Q, Kc, Vc, L, bits, O, w, st)
-                   : run<uint16_t, 128>(c, p, Q, Kc, Vc, L, bits, O, w, st);
+  return c.D == 64 ? run<uint16_t, 64>(c, p, Q, Kc, Vc, L, bits, O, w, st, paged)
+                   : run<uint16_t, 128>(c, p, Q, Kc, Vc, L, bits, O, w, st, paged);
 }
 
 }  // namespace medusa

@@ -135,9 +135,11 @@ __device__ __forceinline__ float exp32(const uint32_t* v, float scale_log2, floa
 
 __global__ void __launch_bounds__(kThreads, 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt,
                     const uint16_t* __restrict__ Q, const int32_t* __restrict__ L, const uint64_t* __restrict__ bits,
                     int N, int Hq, int Hkv, int L_cap, int chunk, float scale_log2, float* __restrict__ o_part,
-                    float* __restrict__ ml_part, uint16_t* __restrict__ O) {
+                    float* __restrict__ ml_part, uint16_t* __restrict__ O, const int32_t* __restrict__ block_table,
+                    int page_rows) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
@@ -245,7 +247,45 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   __syncthreads();
   tc::fence_after();
 
-  if (warp == kProducerWarp) {
+  if (warp == kProducerWarp && page_rows > 0) {
+    // ---------------------------------------------------------- TMA producer, paged
+    // Prefix tile j (keys k_begin + 128 j ..) lies inside one page (page_rows is a
+    // multiple of 128): pool row (page * Hkv + kvh) * page_rows + key % page_rows.
+    // The tree tile comes from the staging buffer, row (b * Hkv + kvh) * N. The
+    // whole warp walks the schedule: every 32 tiles each lane fetches one block-table
+    // entry and lane 0 takes them by shuffle.
+    const int max_pages = L_cap / page_rows;
+    int page_reg = 0, issued = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j % kStages;
+      bool ok = true;
+      if (j >= kStages) ok = tc::mbar_wait<true>(&kv_empty[st], ((j / kStages) - 1) & 1, err, 1);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const bool tree = j >= ptiles;
+      if (!tree && (j & 31) == 0) {
+        const int jj = j + lane;
+        page_reg = jj < ptiles ? block_table[(size_t)b * max_pages + (k_begin + jj * kKeys) / page_rows] : 0;
+      }
+      const int page = __shfl_sync(0xffffffffu, page_reg, j & 31);
+      const int key0 = k_begin + j * kKeys;
+      const int row0 = tree ? (b * Hkv + kvh) * N : (page * Hkv + kvh) * page_rows + key0 % page_rows;
+      if (lane == 0) {
+        const CUtensorMap* mk = tree ? &tmKt : &tmK;
+        const CUtensorMap* mv = tree ? &tmVt : &tmV;
+        uint8_t* dst = ring + st * kStage;
+        tc::mbar_arrive_expect(&kv_full[st], kStage);
+        tc::tma_load_2d(dst, mk, 0, row0, &kv_full[st]);
+        tc::tma_load_2d(dst + kHalf, mk, 64, row0, &kv_full[st]);
+        tc::tma_load_2d(dst + kOperand, mv, 0, row0, &kv_full[st]);
+        tc::tma_load_2d(dst + kOperand + kHalf, mv, 64, row0, &kv_full[st]);
+      }
+      __syncwarp();
+      issued = j + 1;
+    }
+    if (lane == 0)   // drain: never leave the CTA with tile loads still landing in shared memory
+      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+        tc::mbar_wait(&kv_full[j % kStages], (j / kStages) & 1, err, 128);
+  } else if (warp == kProducerWarp) {
     if (lane == 0) {
       // ---------------------------------------------------------------- TMA producer
       const int head_row = (b * Hkv + kvh) * L_cap;
@@ -481,21 +521,32 @@ int attention_tc_ctas_x(int NG) { return attention_tc_mtiles(NG); }
 
 cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, const void* Q, const void* Kc,
                                 const void* Vc, const int32_t* L, const uint64_t* bits, float* o_part, float* ml_part,
-                                void* O, cudaStream_t st) {
+                                void* O, cudaStream_t st, const PagedKV* paged) {
   const TreeShape ts = tree_shape(c);
-  const uint64_t rows = (uint64_t)c.B * c.Hkv * c.L_cap;
-  CUtensorMap tmK, tmV;
-  if (!encode_tmap_2d_bf16(&tmK, Kc, rows, kD, kD * 2, 64, kKeys) ||
-      !encode_tmap_2d_bf16(&tmV, Vc, rows, kD, kD * 2, 64, kKeys))   // boxes of 128 keys x 64 head dims
-    return cudaErrorInvalidValue;
+  CUtensorMap tmK, tmV, tmKt, tmVt;
+  if (paged) {   // pool [pages][Hkv][page_rows][D]; staged tree rows [B][Hkv][N][D]
+    const uint64_t prow = (uint64_t)paged->num_pages * c.Hkv * paged->page_rows, trow = (uint64_t)c.B * c.Hkv * ts.N;
+    if (!encode_tmap_2d_bf16(&tmK, Kc, prow, kD, kD * 2, 64, kKeys) ||
+        !encode_tmap_2d_bf16(&tmV, Vc, prow, kD, kD * 2, 64, kKeys) ||
+        !encode_tmap_2d_bf16(&tmKt, paged->Kt, trow, kD, kD * 2, 64, kKeys) ||
+        !encode_tmap_2d_bf16(&tmVt, paged->Vt, trow, kD, kD * 2, 64, kKeys))
+      return cudaErrorInvalidValue;
+  } else {
+    const uint64_t rows = (uint64_t)c.B * c.Hkv * c.L_cap;
+    if (!encode_tmap_2d_bf16(&tmK, Kc, rows, kD, kD * 2, 64, kKeys) ||
+        !encode_tmap_2d_bf16(&tmV, Vc, rows, kD, kD * 2, 64, kKeys))   // boxes of 128 keys x 64 head dims
+      return cudaErrorInvalidValue;
+    tmKt = tmK;
+    tmVt = tmV;
+  }
   cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)kD));
   const int NG = ts.N * (c.Hq / c.Hkv);
   dim3 grid(attention_tc_mtiles(NG), c.Hkv * c.B, nsplit);
-  launch_pdl(tree_attn_tc_kernel, grid, kThreads, kSmemBytes, st, tmK, tmV, static_cast<const uint16_t*>(Q), L, bits, ts.N, c.Hq,
-                                                     c.Hkv, c.L_cap, chunk, scale_log2, o_part, ml_part,
-                                                     static_cast<uint16_t*>(O));
+  launch_pdl(tree_attn_tc_kernel, grid, kThreads, kSmemBytes, st, tmK, tmV, tmKt, tmVt, static_cast<const uint16_t*>(Q),
+             L, bits, ts.N, c.Hq, c.Hkv, c.L_cap, chunk, scale_log2, o_part, ml_part, static_cast<uint16_t*>(O),
+             paged ? paged->block_table : static_cast<const int32_t*>(nullptr), paged ? paged->page_rows : 0);
   note_launches(1);
   return cudaGetLastError();
 }

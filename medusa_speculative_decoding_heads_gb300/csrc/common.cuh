@@ -120,15 +120,28 @@ cudaError_t launch_tree_build(const medusa_cfg& c, const int32_t* root, const in
                               uint8_t* mask, uint64_t* bits, int32_t* tokens, int32_t* pos,
                               uint32_t* flags, cudaStream_t st);
 
+// A paged KV cache: pool [num_pages][Hkv][page_rows][D] (Kc/Vc point at it),
+// block_table [B][L_cap / page_rows], the tree's rows staged in Kt/Vt [B][Hkv][N][D].
+struct PagedKV {
+  int num_pages, page_rows;
+  const int32_t* block_table;
+  const void* Kt;
+  const void* Vt;
+};
+
 cudaError_t launch_attention(const medusa_cfg& c, const void* Q, const void* Kc, const void* Vc,
-                             const int32_t* L, const uint64_t* bits, void* O, void* ws, cudaStream_t st);
+                             const int32_t* L, const uint64_t* bits, void* O, void* ws, cudaStream_t st,
+                             const PagedKV* paged = nullptr);
+cudaError_t launch_kv_commit_paged(const medusa_cfg& c, void* Kp, void* Vp, const PagedKV& pg, int n_layers,
+                                   size_t pool_layer_elems, size_t tree_layer_elems, int32_t* L, const int32_t* acc,
+                                   const int32_t* path, int32_t* kv_map, cudaStream_t st);
 size_t attention_workspace(const medusa_cfg& c);
 int attention_mma_warps(int NG, int* row_blocks);
 int attention_tc_mtiles(int NG);
 int attention_tc_ctas_x(int NG);
 cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, const void* Q, const void* Kc,
                                 const void* Vc, const int32_t* L, const uint64_t* bits, float* o_part, float* ml_part,
-                                void* O, cudaStream_t st);
+                                void* O, cudaStream_t st, const PagedKV* paged);
 cudaError_t launch_attention_mma(const medusa_cfg& c, int nsplit, int chunk, const void* Q, const void* Kc,
                                  const void* Vc, const int32_t* L, const uint64_t* bits, float* o_part, float* ml_part,
                                  cudaStream_t st);

@@ -74,6 +74,54 @@ kv_compact_kernel(uint4* __restrict__ Kc, uint4* __restrict__ Vc, int Hkv, int r
   }
 }
 
+// Paged cache, every layer: logical row L_b + r (r = 0..acc_b) of sequence b
+// receives the staged tree row path[b][r]; grid (ncta, B) in clusters of ncta
+// CTAs per sequence, CTA `rank` taking (layer, KV head) pairs rank, rank + ncta,
+// ... with one 16-byte column slice per thread and step. Sources (staging) and
+// destinations (pages) never overlap, so no ordering is needed beyond the
+// cluster barrier before CTA 0 writes the KV map and advances L_b.
+__global__ void __launch_bounds__(kCompactThreads)
+kv_commit_paged_kernel(uint4* __restrict__ Kp, uint4* __restrict__ Vp, const uint4* __restrict__ Kt,
+                       const uint4* __restrict__ Vt, const int32_t* __restrict__ block_table, int max_pages,
+                       int page_rows, int n_layers, size_t pool_layer_vec, size_t tree_layer_vec, int Hkv, int row_vec,
+                       int N, int K, int32_t* __restrict__ L, const int32_t* __restrict__ acc,
+                       const int32_t* __restrict__ path, int32_t* __restrict__ kv_map) {
+  pdl_wait();
+  pdl_trigger();
+  const int rank = blockIdx.x, ncta = gridDim.x, b = blockIdx.y;
+  const int Lb = L[b];
+  const int a = acc[b];
+  const bool ok = Lb >= 0 && Lb + N <= max_pages * page_rows && a >= 0 && a <= K;
+  const int32_t* pb = path + (size_t)b * (K + 1);
+  if (ok) {
+    int src[kMaxK + 1];
+    size_t dst[kMaxK + 1];   // pool row of logical row Lb + r, before the head offset
+#pragma unroll
+    for (int r = 0; r <= kMaxK; ++r) {
+      const int sr = r <= a ? pb[r] : 0;
+      src[r] = sr < 0 ? 0 : (sr >= N ? N - 1 : sr);
+      const int row = Lb + (r <= a ? r : 0);
+      dst[r] = (size_t)block_table[(size_t)b * max_pages + row / page_rows] * Hkv * page_rows + row % page_rows;
+    }
+    const int pairs = n_layers * Hkv * 2;              // (layer, head, K or V)
+    for (int i = rank * kCompactThreads + threadIdx.x; i < pairs * row_vec; i += ncta * kCompactThreads) {
+      const int col = i % row_vec, pr = i / row_vec;
+      const int kv = pr & 1, h = (pr >> 1) % Hkv, layer = (pr >> 1) / Hkv;
+      const uint4* sbase = (kv ? Vt : Kt) + layer * tree_layer_vec + ((size_t)b * Hkv + h) * N * row_vec + col;
+      uint4* dbase = (kv ? Vp : Kp) + layer * pool_layer_vec + (size_t)h * page_rows * row_vec + col;
+#pragma unroll
+      for (int r = 0; r <= kMaxK; ++r)
+        if (r <= a) dbase[dst[r] * row_vec] = sbase[(size_t)src[r] * row_vec];
+    }
+  }
+  cluster_barrier();
+  if (rank == 0) {
+    for (int r = threadIdx.x; r <= K; r += kCompactThreads)
+      kv_map[(size_t)b * (K + 1) + r] = (ok && r <= a) ? pb[r] : -1;
+    if (threadIdx.x == 0 && ok) L[b] = Lb + a + 1;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_kv_compact(const medusa_cfg& c, void* Kc, void* Vc, int32_t* L, const int32_t* acc,
@@ -98,6 +146,38 @@ cudaError_t launch_kv_compact(const medusa_cfg& c, void* Kc, void* Vc, int32_t* 
   cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kv_compact_kernel, static_cast<uint4*>(Kc), static_cast<uint4*>(Vc), c.Hkv,
                                      row_vec, c.L_cap, ts.N, c.K, L, acc, path, kv_map);
+  note_launches(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_commit_paged(const medusa_cfg& c, void* Kp, void* Vp, const PagedKV& pg, int n_layers,
+                                   size_t pool_layer_elems, size_t tree_layer_elems, int32_t* L, const int32_t* acc,
+                                   const int32_t* path, int32_t* kv_map, cudaStream_t st) {
+  const TreeShape ts = tree_shape(c);
+  const int elt = c.dtype == MEDUSA_F32 ? 4 : 2;
+  const int row_vec = c.D * elt / 16;
+  const int per16 = 16 / elt;   // elements per 16-byte vector
+  const int work = n_layers * c.Hkv * 2;
+  const int ncta = work < kCompactCluster ? work : kCompactCluster;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ncta, c.B);
+  cfg.blockDim = dim3(kCompactThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ncta;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // as launch_pdl
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kv_commit_paged_kernel, static_cast<uint4*>(Kp), static_cast<uint4*>(Vp),
+                                     static_cast<const uint4*>(pg.Kt), static_cast<const uint4*>(pg.Vt), pg.block_table,
+                                     c.L_cap / pg.page_rows, pg.page_rows, n_layers, pool_layer_elems / per16,
+                                     tree_layer_elems / per16, c.Hkv, row_vec, ts.N, c.K, L, acc, path, kv_map);
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

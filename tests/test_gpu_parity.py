@@ -415,6 +415,101 @@ def test_kv_compact_bit_exact(name):
     assert np.array_equal(i64(Ld), Lr) and np.array_equal(i64(st.kv_map), kv_map)
 
 
+# --------------------------------------------------------------------------- paged cache (NEXT f4)
+def paged_layout(si, w, P, seed):
+    """The committed rows of si.Kc/Vc moved into a shuffled page pool, the tree rows staged."""
+    rng = np.random.default_rng(seed)
+    cap = -(-si.L_cap // P) * P
+    max_pages = cap // P
+    num_pages = w.B * max_pages + 3
+    bt = rng.permutation(num_pages)[:w.B * max_pages].reshape(w.B, max_pages).astype(np.int32)
+    Kc, Vc = si.Kc.cpu(), si.Vc.cpu()
+    Kp = torch.zeros((num_pages, w.Hkv, P, w.D), dtype=Kc.dtype)
+    Vp = torch.zeros_like(Kp)
+    for b in range(w.B):
+        for i in range(int(si.L[b])):
+            Kp[bt[b, i // P], :, i % P] = Kc[b, :, i]
+            Vp[bt[b, i // P], :, i % P] = Vc[b, :, i]
+    Kt = torch.stack([Kc[b, :, int(si.L[b]):int(si.L[b]) + w.N] for b in range(w.B)])
+    Vt = torch.stack([Vc[b, :, int(si.L[b]):int(si.L[b]) + w.N] for b in range(w.B)])
+    return cap, num_pages, bt, Kp, Vp, Kt, Vt
+
+
+@pytest.mark.parametrize("name,P", [("vicuna7b_b1", 128), ("vicuna7b_b1", 256), ("gqa7b_b32", 128),
+                                    ("vicuna13b_b8", 256), ("vicuna7b_b1_pruned64", 128)])
+def test_attention_paged(name, P):
+    """Tree attention with the committed rows in a shuffled page pool and the tree rows
+    staged: the oracle's attention over the same logical cache (lengths 0, one page,
+    ragged; one or several KV splits)."""
+    dev = gpu_ready()
+    w0 = configs.get(name)
+    G = w0.Hq // w0.Hkv
+    w = configs.scaled(w0, B=5 if w0.B > 1 else 1, d=256, V=1000, Hq=2 * G, Hkv=2, L_range=(0, 700))
+    si = synth.make_step_inputs(w, seed=P + 3, device=dev)
+    if w.B > 1:
+        si.L[0], si.L[1] = 0, P      # empty prefix; exactly one page
+    cap, num_pages, bt, Kp, Vp, Kt, Vt = paged_layout(si, w, P, seed=P)
+    st = DeviceStep(w, w.modes[0], cap, dev)
+    Ld = torch.from_numpy(si.L).to(dev)
+    st.tree_build(torch.from_numpy(si.root_token).to(dev), Ld,
+                  topk=torch.zeros((w.B, w.K, w.s_max), dtype=torch.int32, device=dev))
+    O_gpu = torch.empty_like(si.Q)
+    mb.tree_attention_paged(st.cfg, si.Q, Kp.to(dev), Vp.to(dev), num_pages, P, torch.from_numpy(bt).to(dev),
+                            Kt.to(dev), Vt.to(dev), Ld, st.anc_bits, O_gpu, st.workspace)
+    torch.cuda.synchronize()
+    mask = O.ancestor_mask(layout(w)["parent"])
+    pairs = [(b, h) for b in range(w.B) for h in range(w.Hq)]
+    ref = O.tree_attention_paged(f64(si.Q), f64(Kp), f64(Vp), bt, P, f64(Kt), f64(Vt), si.L, mask, w.Hq, w.Hkv,
+                                 pairs=pairs)
+    assert_close(f64(O_gpu), ref, w.dtype, "paged attention")
+
+
+@pytest.mark.parametrize("n_layers,P", [(1, 128), (3, 256)])
+def test_kv_commit_paged_bit_exact(n_layers, P):
+    """The accepted path's staged rows land at logical rows L_b.. of every layer's pages."""
+    dev = gpu_ready()
+    w = configs.scaled(configs.get("vicuna13b_b8"), d=256, V=1000, Hq=4, Hkv=4, L_range=(100, 900))
+    si = synth.make_step_inputs(w, seed=77, device=dev)
+    cap, num_pages, bt, _, _, _, _ = paged_layout(si, w, P, seed=5)
+    rng = np.random.default_rng(6)
+    raw = lambda shape: rng.integers(-30000, 30000, size=shape).astype(np.int16)   # bf16 bit patterns
+    Kp = [raw((num_pages, w.Hkv, P, w.D)) for _ in range(n_layers)]
+    Vp = [raw((num_pages, w.Hkv, P, w.D)) for _ in range(n_layers)]
+    Kt = [raw((w.B, w.Hkv, w.N, w.D)) for _ in range(n_layers)]
+    Vt = [raw((w.B, w.Hkv, w.N, w.D)) for _ in range(n_layers)]
+    tree = layout(w)
+    acc = rng.integers(0, w.K + 1, size=w.B).astype(np.int32)
+    acc[0], acc[-1] = 0, w.K
+    path = np.full((w.B, w.K + 1), -1, dtype=np.int32)
+    for b in range(w.B):
+        cur = 0
+        path[b, 0] = 0
+        for r in range(1, acc[b] + 1):
+            kids = O.children_of(tree["parent"], cur)
+            cur = kids[int(rng.integers(len(kids)))]
+            path[b, r] = cur
+    L = si.L.astype(np.int32).copy()
+    L[2] = cap - w.N + 1                      # no room: left as it is
+    to_dev = lambda arrs: torch.from_numpy(np.stack(arrs)).to(dev)
+    Kpd, Vpd, Ktd, Vtd = to_dev(Kp), to_dev(Vp), to_dev(Kt), to_dev(Vt)
+    st = DeviceStep(w, w.modes[0], cap, dev)
+    Ld = torch.from_numpy(L).to(dev)
+    mb.kv_commit_paged(st.cfg, Kpd, Vpd, P, torch.from_numpy(bt).to(dev), Ktd, Vtd, n_layers, Kp[0].size,
+                       Kt[0].size, Ld, torch.from_numpy(acc).to(dev), torch.from_numpy(path).to(dev), st.kv_map)
+    torch.cuda.synchronize()
+    ok = np.array([0 <= L[b] and L[b] + w.N <= cap for b in range(w.B)])
+    assert not ok[2] and ok.sum() == w.B - 1
+    # the oracle on the sequences with room (each owns its pages, so the others are untouched)
+    kps, vps, L_ok, map_ok = O.kv_commit_paged(Kp, Vp, bt[ok], P, [k[ok] for k in Kt], [v[ok] for v in Vt],
+                                               L[ok], acc[ok], path[ok])
+    L2 = L.astype(np.int64).copy()
+    L2[ok] = L_ok
+    kv_map = np.full((w.B, w.K + 1), -1, dtype=np.int64)
+    kv_map[ok] = map_ok
+    assert np.array_equal(Kpd.cpu().numpy(), np.stack(kps)) and np.array_equal(Vpd.cpu().numpy(), np.stack(vps))
+    assert np.array_equal(i64(Ld), L2) and np.array_equal(i64(st.kv_map), kv_map)
+
+
 # --------------------------------------------------------------------------- whole step
 @pytest.mark.parametrize("name", NAMES + configs.SHARED + configs.PRUNED)
 def test_step_end_to_end_small(name):
