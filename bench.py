@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of one CUDA graph")
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed steps before the timed region")
+    ap.add_argument("--paged", type=int, default=0,
+                    help="with --part attention: rows per page of a shuffled paged pool (0: contiguous cache)")
     ap.add_argument("--part", default="step", choices=["step", "heads", "attention", "verify"],
                     help="diagnostic: time one library call in a loop (for profiler captures)")
     ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
@@ -295,6 +297,29 @@ def run_part(args):
     call = {"heads": lambda: st.heads(si.h, si.W, si.bias, si.U, write_logits=mode == REJECTION),
             "attention": lambda: st.tree_attention(si.Q, si.Kc, si.Vc, L),
             "verify": lambda: st.verify(tl, ua, ur)}[args.part]
+    if args.part == "attention" and args.paged:
+        # the same committed rows in a shuffled page pool, the tree rows staged
+        P = args.paged
+        cap = -(-si.L_cap // P) * P
+        Kc = torch.nn.functional.pad(si.Kc, (0, 0, 0, cap - si.L_cap))
+        Vc = torch.nn.functional.pad(si.Vc, (0, 0, 0, cap - si.L_cap))
+        mp = cap // P
+        gen = torch.Generator(device="cpu")
+        gen.manual_seed(args.seed)
+        perm = torch.randperm(w.B * mp, generator=gen).to(dev)             # pool slot of page (b, i)
+        pool_k = torch.empty((w.B * mp, w.Hkv, P, w.D), dtype=Kc.dtype, device=dev)
+        pool_v = torch.empty_like(pool_k)
+        pool_k[perm] = Kc.view(w.B, w.Hkv, mp, P, w.D).permute(0, 2, 1, 3, 4).reshape(w.B * mp, w.Hkv, P, w.D)
+        pool_v[perm] = Vc.view(w.B, w.Hkv, mp, P, w.D).permute(0, 2, 1, 3, 4).reshape(w.B * mp, w.Hkv, P, w.D)
+        bt = perm.view(w.B, mp).to(torch.int32)
+        Kt = torch.stack([si.Kc[b, :, int(si.L[b]):int(si.L[b]) + w.N] for b in range(w.B)]).contiguous()
+        Vt = torch.stack([si.Vc[b, :, int(si.L[b]):int(si.L[b]) + w.N] for b in range(w.B)]).contiguous()
+        del Kc, Vc
+        st = DeviceStep(w, mode, cap, dev)
+        st.tree_build(torch.from_numpy(si.root_token).to(dev), L)
+        O_out = torch.empty_like(si.Q)
+        call = lambda: mb.tree_attention_paged(st.cfg, si.Q, pool_k, pool_v, w.B * mp, P, bt, Kt, Vt, L,
+                                               st.anc_bits, O_out, st.workspace)
     for _ in range(max(3, args.warmup)):
         call()
     torch.cuda.synchronize()
@@ -305,7 +330,8 @@ def run_part(args):
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / args.steps
-    print(json.dumps({"part": args.part, "workload": w.name, "overrides": args.set, "us_per_call": 1000 * ms}))
+    print(json.dumps({"part": args.part, "workload": w.name, "overrides": args.set, "paged": args.paged,
+                      "us_per_call": 1000 * ms}))
     return 0
 
 
