@@ -133,3 +133,15 @@ def test_malformed_pruned_trees_are_rejected(lib, edit):
     cfg = mb.make_cfg(B=w.B, d=w.d, V=w.V, branching=w.branching, Hq=w.Hq, Hkv=w.Hkv, D=w.D, L_cap=4096,
                       dtype=w.dtype, mode=configs.GREEDY, tree_nodes=(parent, rank))
     assert mb.raw_call("medusa_workspace_size", ctypes.byref(cfg), ctypes.byref(ctypes.c_size_t())) == -1
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without the built library the binding raises instead of falling back to anything."""
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "from medusa_speculative_decoding_heads_gb300 import binding\n"
+            "try:\n    binding.load(%r)\nexcept RuntimeError as e:\n    print('raised:', e)\n    sys.exit(3)\n"
+            % (ROOT, str(tmp_path / "libmedusa.so")))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 3 and "not built" in r.stdout, (r.stdout, r.stderr)
