@@ -40,7 +40,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per medusa_heads call, from the committed ncu capture of the heads
 # kernels on a reduced vocabulary (V=8000: traffic 1.02x the algorithmic
 # weight bytes), scaled to the workload's weight rows. Absent = not captured.
-NCU_TRAFFIC_BYTES = {"vicuna7b_b1": 1189563648, "vicuna7b_b1_shared": 402850048}   # dram read + write of the medusa_heads kernels, one call
+NCU_TRAFFIC_BYTES = {"vicuna7b_b1": 1189250048, "vicuna7b_b1_shared": 402850048}   # dram read + write of the medusa_heads kernels, one call
 
 
 def parse():
