@@ -8,10 +8,13 @@
 // section 3.3: the online-softmax property that makes block-wise partials
 // exact), which lets the committed prefix be split across CTAs.
 //
-// bf16 inputs take the tensor-core partial kernel (attention_mma.cu); this file
-// holds the float32 kernel (CUDA cores, float32 softmax and accumulation), the
-// split plan and the merge: grid (query-row groups, KV head x sequence, KV split). The committed prefix is unmasked; the last split also
-// visits the N tree rows, where the ancestor bitmask is applied in registers.
+// bf16 with D = 128 takes the tcgen05 kernel (attention_tc.cu, which also reads
+// a paged cache through a block table), bf16 with D = 64 the mma.sync kernel
+// (attention_mma.cu). This file holds the float32 kernel (CUDA cores, float32
+// softmax and accumulation), the split plan and the merge: grid (query-row
+// groups, KV head x sequence, KV split). The committed prefix is unmasked; the
+// last split also visits the N tree rows, where the ancestor bitmask is applied
+// in registers.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>

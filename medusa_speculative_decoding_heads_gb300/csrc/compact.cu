@@ -1,4 +1,5 @@
-// KV compaction of the accepted path, in place.
+// KV compaction of the accepted path, in place; and its paged-cache form, which
+// commits the accepted path's staged tree rows into the pages of every layer.
 //
 // "Speculative Decoding 원리와 가속 아키텍처" (blog.huny.dev), section 5 Case 2
 // (rejected drafts are rolled back) and section 6 (the tree verification needs

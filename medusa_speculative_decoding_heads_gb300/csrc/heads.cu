@@ -10,6 +10,9 @@
 // weights stream from HBM exactly once and each weight row meets all B input
 // vectors while it is in registers.
 //
+// The tcgen05 path (heads_tc.cu) serves bf16 with B <= 32 and d % 64 == 0; this
+// file keeps the per-head top-s selection and the paths for other shapes.
+//
 // bf16 path (tensor cores, mma.sync m16n8k16, swap-AB): the weight rows are the
 // 16-row A operand, the batch is the 8-wide B operand. Products of two bf16
 // values are exact in the f32 accumulator, so the d x d layer on the bf16

@@ -9,7 +9,9 @@
 // M dimension (A operand, K-major, straight from the row-major weights), the
 // batch vectors are the N dimension (B operand). The vocab projection consumes
 // the f32 residual as bf16 hi and lo vectors, i.e. N = 2 * NB columns; the two
-// columns of a sequence are added in the epilogue.
+// columns of a sequence are added in the epilogue. When every head shares one
+// frozen vocab projection (the same section's note on W_head^(k)), all heads'
+// hi/lo vectors form one B operand and the projection is streamed once.
 //
 // Persistent CTAs (one per SM) walk a static list of work units (head, 128-row
 // tile, k range). The vocab projection takes whole tiles round robin. The

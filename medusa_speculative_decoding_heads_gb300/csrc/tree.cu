@@ -1,4 +1,5 @@
-// Cartesian candidate tree: layout, ancestor mask, tokens and position ids.
+// Candidate tree (Cartesian, or pruned from a node list): layout, ancestor mask,
+// tokens and position ids.
 //
 // "Medusa 심층 아키텍처" (techknowgenie), section "트리 어텐션": each head keeps its
 // top-s candidates and the candidates of consecutive heads are combined into a
