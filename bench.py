@@ -436,6 +436,10 @@ def run_ours(args):
     clocks = sampler.stop() if sampler else None
     elapsed_ms = t0.elapsed_time(t1)
     per_call = {n: statistics.mean(m[i].elapsed_time(m[i + 1]) for m in marks) for i, n in enumerate(names)}
+    # the spread of single steps, from the event-marked replay (events end the launch overlap, so these
+    # run a little above ms_per_step)
+    q = np.percentile([m[0].elapsed_time(m[-1]) for m in marks], [10, 50, 90])
+    step_spread = {"p10": float(q[0]), "p50": float(q[1]), "p90": float(q[2]), "source": "event-marked replay"}
     heads_ms = per_call["heads"]
     elapsed_ms, value = replica_throughput(elapsed_ms, args.steps, world, dev)
     ms_per_step = elapsed_ms / args.steps
@@ -468,6 +472,7 @@ def run_ours(args):
                           "frac_of_8000_gbs": by["total"] / (ms_per_step * 1e-3) / 1e9 / 8000.0,
                           "bytes_by_term": by},
         "breakdown_ms": dict(per_call, step=ms_per_step),
+        "marked_step_ms": step_spread,
         "launch_mode": launch_mode,
         "accepted_per_step": float(np.mean(acc + 1)),
         "e2e": e2e,

@@ -518,6 +518,37 @@ def test_step_end_to_end_small(name):
     w = small(configs.get(name))
     if w.B < 8:
         w = configs.scaled(w, B=8)
+    check_step(w, dev)
+
+
+def _limit_cases():
+    base = configs.scaled(configs.get("vicuna7b_b1"), B=8, d=512, V=1000, Hq=8, Hkv=2, L_range=(37, 300),
+                          modes=(GREEDY, REJECTION), temperature=0.9)
+    paths = configs.pruned_paths(8, 8, 127)
+    br = tuple(1 + max(p[e] for p in paths if len(p) > e) for e in range(8))
+    return {
+        # 128 nodes (the most the library takes) over 8 heads (the most heads): two full ancestor words,
+        # a 128-key tree tile and 4 query tiles of 128 rows per KV head
+        "pruned128_k8": configs.scaled(base, name="pruned128_k8", branching=br, tree_paths=paths),
+        # top-8 lists (the widest branching) at two depths: 73 nodes
+        "cartesian_8x8": configs.scaled(base, name="cartesian_8x8", branching=(8, 8), Hq=4, Hkv=4),
+        # a chain of 8 heads with one candidate each, 64-dim heads (the mma.sync attention)
+        "chain_k8_d64": configs.scaled(base, name="chain_k8_d64", branching=(1,) * 8, D=64, Hq=6, Hkv=2),
+        # more sequences than the tcgen05 heads plan takes (the mma.sync heads path)
+        "batch40": configs.scaled(base, name="batch40", B=40, branching=(3, 2, 2)),
+    }
+
+
+@pytest.mark.parametrize("case", ["pruned128_k8", "cartesian_8x8", "chain_k8_d64", "batch40"])
+def test_step_at_limits(case):
+    """The whole step at the library's limits: 128 nodes, 8 heads, top-8 lists, batches past the tcgen05 plan."""
+    dev = gpu_ready()
+    w = _limit_cases()[case]
+    assert w.N <= 128 and w.K <= 8 and max(w.branching) <= 8
+    check_step(w, dev)
+
+
+def check_step(w, dev):
     for mode in w.modes:
         si = synth.make_step_inputs(w, seed=31, device=dev, with_bias=True)
         r, z = O.medusa_heads(f64(si.h), f64(si.W), f64(si.bias), f64(si.U))
