@@ -128,9 +128,10 @@ MEDUSA_API int medusa_workspace_size(const medusa_cfg* cfg, size_t* bytes);
  *                              `head_logits` by medusa_verify in MEDUSA_REJECTION.
  *   topk   [B][K][s_max] int32 indices of the s_k largest z_k entries, descending,
  *                              ties to the lower index; -1 beyond s_k.
- * r_k is kept in float32; accumulation is float32. bf16 needs d % 64 == 0 and
- * B <= 32 (MEDUSA_ERR_UNSUPPORTED otherwise) and 16-byte aligned h, W, bias
- * and U (MEDUSA_ERR_INVALID_ARG otherwise). */
+ * r_k is kept in float32; accumulation is float32. bf16 needs d % 64 == 0
+ * (MEDUSA_ERR_UNSUPPORTED otherwise) and 16-byte aligned h, W, bias and U
+ * (MEDUSA_ERR_INVALID_ARG otherwise); a bf16 batch above 32 sequences runs as
+ * consecutive slices of at most 32, each streaming W and U once. */
 MEDUSA_API int medusa_heads(const medusa_cfg* cfg, const void* h, const void* W, const void* bias,
                  const void* U, float* logits, int32_t* topk, void* workspace,
                  medusa_stream_t stream);

@@ -97,11 +97,24 @@ int medusa_heads(const medusa_cfg* cfg, const void* h, const void* W, const void
   if (!h || !W || !U || !topk || !workspace) return MEDUSA_ERR_INVALID_ARG;
   if (!logits && cfg->mode == MEDUSA_REJECTION) return MEDUSA_ERR_INVALID_ARG;
   if (cfg->dtype == MEDUSA_BF16) {
-    if (cfg->d % 64 != 0 || cfg->B > 32) return MEDUSA_ERR_UNSUPPORTED;
+    if (cfg->d % 64 != 0) return MEDUSA_ERR_UNSUPPORTED;
     if (!aligned16(h) || !aligned16(W) || !aligned16(U) || (bias && !aligned16(bias))) return MEDUSA_ERR_INVALID_ARG;
   }
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MEDUSA_ERR_INVALID_ARG;
-  return from_cuda(launch_heads(*cfg, h, W, bias, U, logits, topk, workspace, (cudaStream_t)stream));
+  // bf16 batches run as consecutive slices of at most kHeadsBatch sequences (the
+  // GEMVs' widest batch operand), each streaming the weights once.
+  const int slice = cfg->dtype == MEDUSA_BF16 ? kHeadsBatch : cfg->B;
+  const size_t h_row = (size_t)cfg->d * (cfg->dtype == MEDUSA_BF16 ? 2 : 4);
+  const TreeShape ts = tree_shape(*cfg);
+  for (int b0 = 0; b0 < cfg->B; b0 += slice) {
+    medusa_cfg c = *cfg;
+    c.B = cfg->B - b0 < slice ? cfg->B - b0 : slice;
+    cudaError_t e = launch_heads(c, static_cast<const char*>(h) + b0 * h_row, W, bias, U,
+                                 logits ? logits + (size_t)b0 * cfg->K * cfg->V : nullptr,
+                                 topk + (size_t)b0 * cfg->K * ts.s_max, workspace, (cudaStream_t)stream);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return MEDUSA_OK;
 }
 
 int medusa_tree_build(const medusa_cfg* cfg, const int32_t* root_token, const int32_t* topk, const int32_t* L,

@@ -35,6 +35,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 constexpr int kMaxK = 8;
 constexpr int kMaxS = 8;
 constexpr int kMaxN = 128;
+constexpr int kHeadsBatch = 32;   // sequences per bf16 heads pass (larger batches run in slices)
 
 // Tree shape derived from the configuration: level counts and offsets.
 struct TreeShape {

@@ -105,9 +105,10 @@ def test_heads_small(name, with_bias):
     check_heads(w, si, st)
 
 
-@pytest.mark.parametrize("B", [1, 3, 9, 17, 32])
+@pytest.mark.parametrize("B", [1, 3, 9, 17, 32, 33, 70])
 def test_heads_batch_tiles(B):
-    """Every batch tiling of the tensor-core path (1, 2 and 4 tiles of 8) with ragged batches."""
+    """Every batch tiling of the tensor-core path (1, 2 and 4 tiles of 8) with ragged batches, and batches
+    past 32 sequences (run as slices of 32, the last one ragged)."""
     dev = gpu_ready()
     w = configs.scaled(configs.get("vicuna7b_b1"), B=B, d=320, V=700, L_range=(40, 40), Hq=2, Hkv=2)
     si = synth.make_step_inputs(w, seed=B, device=dev, with_bias=True)
@@ -534,7 +535,7 @@ def _limit_cases():
         "cartesian_8x8": configs.scaled(base, name="cartesian_8x8", branching=(8, 8), Hq=4, Hkv=4),
         # a chain of 8 heads with one candidate each, 64-dim heads (the mma.sync attention)
         "chain_k8_d64": configs.scaled(base, name="chain_k8_d64", branching=(1,) * 8, D=64, Hq=6, Hkv=2),
-        # more sequences than the tcgen05 heads plan takes (the mma.sync heads path)
+        # more sequences than one tcgen05 heads pass takes (the heads call runs two batch slices)
         "batch40": configs.scaled(base, name="batch40", B=40, branching=(3, 2, 2)),
     }
 
