@@ -6,7 +6,7 @@
 // the running maximum and exp-sum ("최적화 2편" (beengineer500), section 3.3).
 //
 // One CTA = one 128-row Q tile (tree nodes x query heads of one KV head) against
-// one KV range of one sequence, in tiles of 128 keys. 19 warps:
+// one KV range of one sequence, in tiles of 128 keys. 23 warps:
 //   warp 16 TMA producer: K and V tiles (two 64-column boxes each, 128-byte
 //           swizzle) into a 3-stage ring; allocates TMEM.
 //   warp 17 S issuer: S_j = Q K_j^T (Q held in TMEM, K from shared memory) into
@@ -19,6 +19,14 @@
 //           tile maxima (rounded up to bf16, so that all take exactly the same
 //           running max) once per tile; the running max moves (and O is
 //           rescaled) only on a jump of more than 2^8.
+//   warps 19-22 leftover rows: when the query rows of a KV head end in a short
+//           remainder of at most 8 rows (4 rows for 65 nodes x 4 heads), the
+//           last full tile's CTA carries them instead of a CTA of its own, with
+//           transposed narrow products on the same K/V tiles: S'^T = K Q'^T
+//           (M = 128 keys, N = 16 rows) right behind S_j, and O'^T += V^T P'^T
+//           (M = 128 head dims) right behind PV_j, whose completion frees the
+//           stage. Q' and P' sit in shared memory. Thread = key (S') or head dim
+//           (O'); row maxima cross the four warps through shared memory.
 // Every mbarrier wait is bounded (a few seconds of clock cycles); on expiry the
 // thread records a code in a device error word and leaves its loop.
 #include <cuda.h>
@@ -47,23 +55,43 @@ constexpr int kStage = 2 * kOperand;        // K + V of one key tile
 constexpr int kStages = 3;
 constexpr int kGroups = 4;                  // softmax warpgroups, 32 keys each
 constexpr int kXchg = kGroups * kRows * 4;   // exp-sums [group][row] for the epilogue (2 KB)
-constexpr int kSmemBytes = kStages * kStage + kXchg + 1024;   // + alignment slack
+constexpr int kXRows = 16;                   // N of the narrow products (the smallest N with M = 128)
+constexpr int kXMax = 8;                     // leftover query rows one CTA carries (rows kXMax.. of Q', P' stay 0)
+constexpr int kXHalf = kXRows * 128;         // 16 rows x 64 bf16, one 128-byte-swizzled half (2 KB)
+// shared memory: K/V ring | Q' [16 rows][128 dims] | P' two slots [16 rows][128 keys] | exp-sums | leftover-row
+// reductions (maxima [2][4 warps][16], sums [4 warps][16])
+constexpr int kOffQx = kStages * kStage;
+constexpr int kOffPx = kOffQx + 2 * kXHalf;
+constexpr int kOffXl = kOffPx + 4 * kXHalf;
+constexpr int kOffRed = kOffXl + kXchg;
+constexpr int kSmemBytes = kOffRed + 1024 + 1024;   // + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSoftmaxWarps = 4 * kGroups;
 constexpr int kProducerWarp = 16;
-constexpr int kMmaSWarp = 17;   // issues S = Q K^T
-constexpr int kMmaPWarp = 18;   // issues O += P V
-constexpr int kThreads = 19 * 32;
+constexpr int kMmaSWarp = 17;   // issues S = Q K^T (and S'^T = K Q'^T)
+constexpr int kMmaPWarp = 18;   // issues O += P V (and O'^T += V^T P'^T)
+constexpr int kXWarp0 = 19;     // warps 19-22: softmax of the leftover rows
+constexpr int kThreads = 23 * 32;
 constexpr int kSortMax = 256;   // batches up to this size are taken longest sequence first
 
 // TMEM columns: two S tiles (128 f32 columns each; warpgroup q writes P of its
 // keys [32q, 32q + 32) as bf16 pairs over columns [32q, 32q + 16)), the O
-// accumulator (128 f32 columns), Q as bf16 pairs (64 columns) and the per-tile
-// maxima of the four warpgroups (columns 4 * (tile parity) + group).
+// accumulator (128 f32 columns), Q as bf16 pairs (64 columns), the per-tile
+// maxima of the four warpgroups (columns 4 * (tile parity) + group) and the
+// leftover rows' two S'^T tiles and O'^T accumulator (16 columns each).
 __host__ __device__ constexpr uint32_t col_S(int slot) { return 128u * slot; }
 constexpr uint32_t kColO = 256;
 constexpr uint32_t kColQ = 384;
 constexpr uint32_t kColX = 448;
+constexpr uint32_t kColS2 = 464;   // two S'^T tiles of 16 columns (lane = key, column = leftover row)
+constexpr uint32_t kColO2 = 496;   // O'^T (lane = head dim, column = leftover row)
+
+// Query rows past the last full 128-row tile that the last tile's CTA carries:
+// a remainder of 1..8 rows after at least one full tile, else none.
+__host__ __device__ inline int extra_rows(int NG) {
+  const int r = NG % kRows;
+  return (NG > kRows && r > 0 && r <= kXMax) ? r : 0;
+}
 
 // The running maximum is only moved (and O rescaled) when a tile's maximum
 // exceeds it by more than this many binary orders of magnitude; in between, P
@@ -145,8 +173,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = sm;                                                    // [stage][K | V]
-  float* xl = reinterpret_cast<float*>(sm + kStages * kStage);   // [group][row] exp-sums
+  float* xl = reinterpret_cast<float*>(sm + kOffXl);   // [group][row] exp-sums
   __shared__ __align__(8) uint64_t kv_full[kStages], kv_empty[kStages], s_full[2], p_full[2], p_free[2], xbar;
+  __shared__ __align__(8) uint64_t s2_full[2], p2_full[2], p2_free[2], xbar2;   // leftover rows
   __shared__ uint32_t tmem_slot;
   __shared__ int seq;
   uint32_t* err = &g_attention_tc_error;
@@ -173,6 +202,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = Hq / Hkv, NG = N * G;
+  const int R = (mt == (int)gridDim.x - 1) ? extra_rows(NG) : 0;   // leftover rows this CTA carries
+  const bool xtra = R > 0;
+  const bool xs = xtra && warp >= kXWarp0 && warp < kXWarp0 + 4;   // a leftover-row softmax thread
+  const int xt = 32 * (warp & 3) + lane;     // its TMEM lane: key of S'^T, head dim of O'^T
+  const int xq0 = kRows * (mt + 1);          // query row index of leftover row 0
   const int Lb = L[b];
   const bool valid = Lb >= 0 && Lb + N <= L_cap;
   const int k_begin = split * chunk;
@@ -204,6 +238,18 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         ml_part[2 * orow + 1] = 0.f;
       }
     }
+    if (xs) {
+      for (int r = 0; r < R; ++r) {
+        const int xqi = xq0 + r, xnode = xqi / G, xqh = kvh * G + xqi % G;
+        const size_t orow = (((size_t)b * nsplit + split) * N + xnode) * Hq + xqh;
+        if (nsplit == 1) {
+          O[(((size_t)b * N + xnode) * Hq + xqh) * kD + xt] = 0;
+        } else if (xt == 0) {
+          ml_part[2 * orow] = -INFINITY;
+          ml_part[2 * orow + 1] = 0.f;
+        }
+      }
+    }
     return;
   }
 
@@ -218,6 +264,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       tc::mbar_init(&p_free[i], 1);
     }
     tc::mbar_init(&xbar, kSoftmaxWarps * 32);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&s2_full[i], 1);
+      tc::mbar_init(&p2_full[i], 128);
+      tc::mbar_init(&p2_free[i], 1);
+    }
+    tc::mbar_init(&xbar2, 128);
     tc::mbar_fence_init();
   }
   if (warp == kProducerWarp) tc::tmem_alloc(&tmem_slot, kTmemCols);
@@ -242,6 +294,22 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     }
     tc::tmem_st16(tQ + lane_base + 16 * q, qv);
     tc::tmem_wait_st();
+  }
+  if (xs) {
+    // Q' (the B operand of S'^T = K Q'^T) into shared memory: [16 rows][128 dims], K-major,
+    // two 64-dim halves, 128-byte swizzle; rows past R and both P' slots are zeroed.
+    for (int c = xt; c < kXRows * 16; c += 128) {
+      const int r = c >> 4, ch = c & 15;   // row, 16-byte chunk (8 dims) along D
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < R) {
+        const int xqi = xq0 + r;
+        v = *reinterpret_cast<const uint4*>(Q + (((size_t)b * N + xqi / G) * Hq + kvh * G + xqi % G) * kD + 8 * ch);
+      }
+      *reinterpret_cast<uint4*>(sm + kOffQx + (ch >> 3) * kXHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = v;
+    }
+    for (int c = xt; c < 4 * kXHalf / 16; c += 128)
+      reinterpret_cast<uint4*>(sm + kOffPx)[c] = make_uint4(0, 0, 0, 0);
+    tc::fence_proxy_async();
   }
   tc::fence_before();
   __syncthreads();
@@ -310,7 +378,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     // ------------------------------------------------------------------ S issuer
     // The whole warp walks the schedule (uniform waits); one elected lane issues.
     constexpr uint32_t idS = tc::idesc_bf16_f32(kRows, kKeys, 0, 0);
+    constexpr uint32_t idS2 = tc::idesc_bf16_f32(kKeys, kXRows, 0, 0);
     const uint64_t dK = tc::sw128_desc(tc::saddr(ring), 16, 1024);
+    const uint64_t dQx = tc::sw128_desc(tc::saddr(sm + kOffQx), 16, 1024);
     for (int j = 0; j < ntiles; ++j) {
       const int slot = j & 1, st = j % kStages;
       bool ok = tc::mbar_wait<true>(&kv_full[st], (j / kStages) & 1, err, 2);
@@ -328,13 +398,51 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         tc::commit(&s_full[slot]);
       }
       __syncwarp();
+      if (xtra) {
+        // S'^T_j = K_j Q'^T, once PV'_{j-2} completed: its softmax had read S' slot j & 1, and
+        // P' slot j & 1 is free for the softmax of tile j
+        if (j >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait<true>(&p2_free[slot], ((j >> 1) - 1) & 1, err, 1024)))
+          break;
+        tc::fence_after();
+        if (tc::elect_one()) {
+          const uint64_t a0 = dK + (uint64_t)((st * kStage) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+            const uint32_t offx = ((kk >> 2) * kXHalf + (kk & 3) * 32) >> 4;
+            tc::mma_bf16(tmem + kColS2 + 16 * slot, a0 + off, dQx + offx, idS2, kk > 0);
+          }
+          tc::commit(&s2_full[slot]);
+        }
+        __syncwarp();
+      }
     }
   } else if (warp == kMmaPWarp) {
     // ------------------------------------------------------------------ PV issuer
     // S_j completed before P_j was released, so the completion of PV_j also
     // covers every read of the stage's K tile.
     constexpr uint32_t idPV = tc::idesc_bf16_f32(kRows, kD, 0, 1);
+    constexpr uint32_t idPV2 = tc::idesc_bf16_f32(kD, kXRows, 1, 0);   // A = V^T (MN-major), B = P' (K-major)
     const uint64_t dV = tc::sw128_desc(tc::saddr(ring + kOperand), kHalf, 1024);   // MN-major: LBO = 64-column half
+    const uint64_t dPx = tc::sw128_desc(tc::saddr(sm + kOffPx), 16, 1024);
+    // O'^T += V_t^T P'_t^T once the leftover softmax of tile t has arrived; it also frees the stage
+    auto issue_pv2 = [&](int t) {
+      if (!__all_sync(0xffffffffu, tc::mbar_wait<true>(&p2_full[t & 1], (t >> 1) & 1, err, 2048))) return false;
+      tc::fence_after();
+      if (tc::elect_one()) {
+        const uint64_t a0 = dV + (uint64_t)(((t % kStages) * kStage) >> 4);
+        const uint64_t p0 = dPx + (uint64_t)(((t & 1) * 2 * kXHalf) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint32_t offx = ((kk >> 2) * kXHalf + (kk & 3) * 32) >> 4;
+          tc::mma_bf16(tmem + kColO2, a0 + (uint64_t)((kk * 2048) >> 4), p0 + offx, idPV2, (t > 0 || kk > 0) ? 1 : 0);
+        }
+        tc::commit(&p2_free[t & 1]);
+        tc::commit(&kv_empty[t % kStages]);
+      }
+      __syncwarp();
+      return true;
+    };
     for (int j = 0; j < ntiles; ++j) {
       const int slot = j & 1, st = j % kStages;
       const bool ok = tc::mbar_wait<true>(&p_full[slot], (j >> 1) & 1, err, 8);
@@ -347,9 +455,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           tc::mma_bf16_tmem_a(tmem + kColO, tmem + col_S(slot) + 32 * (kk >> 1) + 8 * (kk & 1),
                               b0 + (uint64_t)((kk * 2048) >> 4), idPV, (j > 0 || kk > 0) ? 1 : 0);
         tc::commit(&p_free[slot]);
-        tc::commit(&kv_empty[st]);
+        if (!xtra) tc::commit(&kv_empty[st]);
       }
       __syncwarp();
+      if (xtra && !issue_pv2(j)) break;
     }
   } else if (smx) {
     // ------------------------------------------------------------------ softmax
@@ -481,6 +590,152 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         }
       }
     }
+  } else if (xs) {
+    // ------------------------------------------------------- leftover-row softmax
+    // Thread xt holds key xt of S'^T (one score per leftover row) and head dim xt of
+    // O'^T. Row maxima: warp shuffles, then the four warps' values through shared
+    // memory (double-buffered by tile parity, one mbarrier phase per tile).
+    const uint32_t xl_base = (uint32_t)(32 * (warp & 3)) << 16;
+    float* red = reinterpret_cast<float*>(sm + kOffRed);   // maxima [parity][warp][row], then sums [warp][row]
+    float m_run[kXMax], l_t[kXMax], corr[kXMax];
+#pragma unroll
+    for (int r = 0; r < kXMax; ++r) {
+      m_run[r] = -INFINITY;
+      l_t[r] = 0.f;
+    }
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int slot = j & 1;
+      ok = tc::mbar_wait(&s2_full[slot], (j >> 1) & 1, err, 4096);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after();
+      uint32_t v[kXMax];
+      tc::tmem_ld8(tmem + kColS2 + 16 * slot + xl_base, v);
+      tc::tmem_wait_ld();
+      const bool tree = j >= ptiles;
+      const int nkeys = tree ? N : min(kKeys, k_end - (k_begin + j * kKeys));
+      float x[kXMax];
+#pragma unroll
+      for (int r = 0; r < kXMax; ++r) {
+        bool vis = r < R && xt < nkeys;
+        if (vis && tree) vis = (bits[2 * ((xq0 + r) / G) + (xt >> 6)] >> (xt & 63)) & 1ull;
+        x[r] = vis ? __uint_as_float(v[r]) * scale_log2 : -INFINITY;
+      }
+      float* rm = red + 64 * slot;
+#pragma unroll
+      for (int r = 0; r < kXMax; ++r) {
+        if (r < R) {
+          float m = x[r];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (lane == 0) rm[16 * (warp & 3) + r] = m;
+        }
+      }
+      tc::mbar_arrive(&xbar2);
+      ok = tc::mbar_wait(&xbar2, j & 1, err, 8192);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      bool any = false;
+#pragma unroll
+      for (int r = 0; r < kXMax; ++r) {
+        corr[r] = 1.f;
+        if (r < R) {
+          const float m_tile = fmaxf(fmaxf(rm[r], rm[16 + r]), fmaxf(rm[32 + r], rm[48 + r]));
+          if (m_tile > m_run[r] + kLazy) {   // also on the first tile (m_run = -inf): corr = 0
+            corr[r] = tc::ex2(m_run[r] - m_tile);
+            m_run[r] = m_tile;
+            any = true;
+          }
+        }
+      }
+      // P' row r, key xt -> the B operand of O'^T += V^T P'^T ([row][key], K-major, 128-byte
+      // swizzle, two 64-key halves). Its slot last fed PV'_{j-2}, complete before S'_j.
+      uint8_t* pr = sm + kOffPx + slot * 2 * kXHalf + (xt >> 6) * kXHalf;
+      const int cc = xt & 63;
+#pragma unroll
+      for (int r = 0; r < kXMax; ++r) {
+        if (r < R) {
+          const float pv = x[r] == -INFINITY ? 0.f : tc::ex2(x[r] - m_run[r]);
+          l_t[r] = l_t[r] * corr[r] + pv;
+          uint16_t hv;
+          asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(hv) : "f"(pv));
+          *reinterpret_cast<uint16_t*>(pr + r * 128 + ((((cc >> 3) ^ (r & 7)) << 4) | ((cc & 7) << 1))) = hv;
+        }
+      }
+      if (j >= 1 && any) {
+        // rescale O'^T once PV'_{j-1} has landed (thread = head dim, column = row)
+        ok = tc::mbar_wait(&p2_free[(j - 1) & 1], ((j - 1) >> 1) & 1, err, 16384);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+        uint32_t ov[kXMax];
+        tc::tmem_ld8(tmem + kColO2 + xl_base, ov);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int r = 0; r < kXMax; ++r) ov[r] = __float_as_uint(__uint_as_float(ov[r]) * corr[r]);
+        tc::tmem_st8(tmem + kColO2 + xl_base, ov);
+      }
+      tc::fence_proxy_async();   // the P' stores, visible to the tensor core
+      tc::tmem_wait_st();
+      tc::fence_before();
+      tc::mbar_arrive(&p2_full[slot]);
+    }
+    if (ok) ok = tc::mbar_wait(&p2_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, err, 32768);
+    const bool have = __all_sync(0xffffffffu, ok);
+    tc::fence_after();
+    // row sums over the 128 key lanes
+    float* rs = red + 128;
+#pragma unroll
+    for (int r = 0; r < kXMax; ++r) {
+      if (r < R) {
+        float t = l_t[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0) rs[16 * (warp & 3) + r] = t;
+      }
+    }
+    tc::mbar_arrive(&xbar2);
+    const bool summed = tc::mbar_wait(&xbar2, ntiles & 1, err, 65536);
+    uint32_t ov[kXMax];
+    if (have) {   // warp-uniform: the TMEM load is a collective of the warp
+      tc::tmem_ld8(tmem + kColO2 + xl_base, ov);
+      tc::tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int r = 0; r < kXMax; ++r) ov[r] = 0u;
+    }
+    for (int r = 0; r < R; ++r) {
+      const float l_tot = summed ? (rs[r] + rs[16 + r]) + (rs[32 + r] + rs[48 + r]) : 0.f;
+      const int xqi = xq0 + r, xnode = xqi / G, xqh = kvh * G + xqi % G;
+      float o = 0.f;
+#pragma unroll
+      for (int u = 0; u < kXMax; ++u)
+        if (u == r) o = __uint_as_float(ov[u]);   // register arrays take compile-time indexes
+      if (nsplit == 1) {
+        const float inv = (have && l_tot > 0.f) ? 1.f / l_tot : 0.f;
+        uint16_t hv;
+        asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(hv) : "f"(o * inv));
+        O[(((size_t)b * N + xnode) * Hq + xqh) * kD + xt] = hv;
+      } else {
+        const size_t orow = (((size_t)b * nsplit + split) * N + xnode) * Hq + xqh;
+        o_part[orow * kD + xt] = o;
+        if (xt == 0) {
+          float mr = -INFINITY;
+#pragma unroll
+          for (int u = 0; u < kXMax; ++u)
+            if (u == r) mr = m_run[u];
+          ml_part[2 * orow] = have ? mr : -INFINITY;
+          ml_part[2 * orow + 1] = have ? l_tot : 0.f;
+        }
+      }
+    }
   }
 
   tc::fence_before();
@@ -516,7 +771,8 @@ bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int attention_tc_mtiles(int NG) { return (NG + kRows - 1) / kRows; }
+// Q-tile CTAs per (sequence, KV head): a short remainder rides with the last full tile.
+int attention_tc_mtiles(int NG) { return NG / kRows + ((NG % kRows != 0 && extra_rows(NG) == 0) ? 1 : 0); }
 int attention_tc_ctas_x(int NG) { return attention_tc_mtiles(NG); }
 
 cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, const void* Q, const void* Kc,
