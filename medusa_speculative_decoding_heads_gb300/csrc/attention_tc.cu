@@ -6,7 +6,7 @@
 // the running maximum and exp-sum ("최적화 2편" (beengineer500), section 3.3).
 //
 // One CTA = one 128-row Q tile (tree nodes x query heads of one KV head) against
-// one KV range of one sequence, in tiles of 128 keys. 23 warps:
+// one KV range of one sequence, in tiles of 128 keys. 19 warps (23 with leftover rows):
 //   warp 16 TMA producer: K and V tiles (two 64-column boxes each, 128-byte
 //           swizzle) into a 3-stage ring; allocates TMEM.
 //   warp 17 S issuer: S_j = Q K_j^T (Q held in TMEM, K from shared memory) into
@@ -71,7 +71,8 @@ constexpr int kProducerWarp = 16;
 constexpr int kMmaSWarp = 17;   // issues S = Q K^T (and S'^T = K Q'^T)
 constexpr int kMmaPWarp = 18;   // issues O += P V (and O'^T += V^T P'^T)
 constexpr int kXWarp0 = 19;     // warps 19-22: softmax of the leftover rows
-constexpr int kThreads = 23 * 32;
+// 19 warps; 23 for configurations whose query rows per KV head end in a short remainder
+__host__ __device__ constexpr int threads_of(bool fold) { return (fold ? 23 : 19) * 32; }
 constexpr int kSortMax = 256;   // batches up to this size are taken longest sequence first
 
 // TMEM columns: two S tiles (128 f32 columns each; warpgroup q writes P of its
@@ -161,7 +162,8 @@ __device__ __forceinline__ float exp32(const uint32_t* v, float scale_log2, floa
   return a.x + a.y;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kFold>
+__global__ void __launch_bounds__(threads_of(kFold), 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt,
                     const uint16_t* __restrict__ Q, const int32_t* __restrict__ L, const uint64_t* __restrict__ bits,
@@ -202,7 +204,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = Hq / Hkv, NG = N * G;
-  const int R = (mt == (int)gridDim.x - 1) ? extra_rows(NG) : 0;   // leftover rows this CTA carries
+  const int R = (kFold && mt == (int)gridDim.x - 1) ? extra_rows(NG) : 0;   // leftover rows this CTA carries
   const bool xtra = R > 0;
   const bool xs = xtra && warp >= kXWarp0 && warp < kXWarp0 + 4;   // a leftover-row softmax thread
   const int xt = 32 * (warp & 3) + lane;     // its TMEM lane: key of S'^T, head dim of O'^T
@@ -795,12 +797,14 @@ cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, cons
     tmKt = tmK;
     tmVt = tmV;
   }
-  cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
   const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)kD));
   const int NG = ts.N * (c.Hq / c.Hkv);
+  const bool fold = extra_rows(NG) > 0;
+  auto kernel = fold ? tree_attn_tc_kernel<true> : tree_attn_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
   dim3 grid(attention_tc_mtiles(NG), c.Hkv * c.B, nsplit);
-  launch_pdl(tree_attn_tc_kernel, grid, kThreads, kSmemBytes, st, tmK, tmV, tmKt, tmVt, static_cast<const uint16_t*>(Q),
+  launch_pdl(kernel, grid, threads_of(fold), kSmemBytes, st, tmK, tmV, tmKt, tmVt, static_cast<const uint16_t*>(Q),
              L, bits, ts.N, c.Hq, c.Hkv, c.L_cap, chunk, scale_log2, o_part, ml_part, static_cast<uint16_t*>(O),
              paged ? paged->block_table : static_cast<const int32_t*>(nullptr), paged ? paged->page_rows : 0);
   note_launches(1);
