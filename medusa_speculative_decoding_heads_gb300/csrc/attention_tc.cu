@@ -58,13 +58,14 @@ constexpr int kXchg = kGroups * kRows * 4;   // exp-sums [group][row] for the ep
 constexpr int kXRows = 16;                   // N of the narrow products (the smallest N with M = 128)
 constexpr int kXMax = 8;                     // leftover query rows one CTA carries (rows kXMax.. of Q', P' stay 0)
 constexpr int kXHalf = kXRows * 128;         // 16 rows x 64 bf16, one 128-byte-swizzled half (2 KB)
-// shared memory: K/V ring | Q' [16 rows][128 dims] | P' two slots [16 rows][128 keys] | exp-sums | leftover-row
-// reductions (maxima [2][4 warps][16], sums [4 warps][16])
-constexpr int kOffQx = kStages * kStage;
+// shared memory: K/V ring | exp-sums | and with leftover rows: Q' [16 rows][128 dims] | P' two slots
+// [16 rows][128 keys] | their reductions (maxima [2][4 warps][16], sums [4 warps][16])
+constexpr int kOffXl = kStages * kStage;
+constexpr int kOffQx = kOffXl + kXchg;   // 1024-byte aligned, as the swizzled operands need
 constexpr int kOffPx = kOffQx + 2 * kXHalf;
-constexpr int kOffXl = kOffPx + 4 * kXHalf;
-constexpr int kOffRed = kOffXl + kXchg;
-constexpr int kSmemBytes = kOffRed + 1024 + 1024;   // + alignment slack
+constexpr int kOffRed = kOffPx + 4 * kXHalf;
+__host__ __device__ constexpr int smem_of(bool fold) { return (fold ? kOffRed + 1024 : kOffQx) + 1024; }   // + alignment slack
+static_assert(kOffQx % 1024 == 0 && kOffPx % 1024 == 0, "swizzled operands start on 1024-byte boundaries");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSoftmaxWarps = 4 * kGroups;
 constexpr int kProducerWarp = 16;
@@ -801,10 +802,10 @@ cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, cons
   const int NG = ts.N * (c.Hq / c.Hkv);
   const bool fold = extra_rows(NG) > 0;
   auto kernel = fold ? tree_attn_tc_kernel<true> : tree_attn_tc_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_of(fold));
   if (e != cudaSuccess) return e;
   dim3 grid(attention_tc_mtiles(NG), c.Hkv * c.B, nsplit);
-  launch_pdl(kernel, grid, threads_of(fold), kSmemBytes, st, tmK, tmV, tmKt, tmVt, static_cast<const uint16_t*>(Q),
+  launch_pdl(kernel, grid, threads_of(fold), smem_of(fold), st, tmK, tmV, tmKt, tmVt, static_cast<const uint16_t*>(Q),
              L, bits, ts.N, c.Hq, c.Hkv, c.L_cap, chunk, scale_log2, o_part, ml_part, static_cast<uint16_t*>(O),
              paged ? paged->block_table : static_cast<const int32_t*>(nullptr), paged ? paged->page_rows : 0);
   note_launches(1);
