@@ -66,7 +66,7 @@ enum {
   MEDUSA_ERR_UNSUPPORTED = -2, /* valid but outside the built limits          */
   MEDUSA_ERR_CAPACITY = -3,    /* host-visible capacity violation              */
   MEDUSA_ERR_CUDA = -4,        /* a CUDA launch or attribute call failed       */
-  MEDUSA_ERR_TIMEOUT = -5      /* reserved: a bounded device-side wait expired */
+  MEDUSA_ERR_TIMEOUT = -5      /* a bounded device-side wait expired (medusa_poll_errors) */
 };
 
 /* Per-sequence flag bits (uint32). */
@@ -208,8 +208,8 @@ MEDUSA_API int medusa_verify(const medusa_cfg* cfg, const int32_t* tokens, const
 MEDUSA_API int medusa_kv_compact(const medusa_cfg* cfg, void* Kc, void* Vc, int32_t* L, const int32_t* acc,
                       const int32_t* path, int32_t* kv_map, medusa_stream_t stream);
 
-/* Tree attention over a paged KV cache (R15 of the design
- * notes: a page pool is a storage layout of the same logical cache).
+/* Tree attention over a paged KV cache. A page pool is read as a storage
+ * layout of the same logical cache that medusa_tree_attention takes.
  *   Kp, Vp [num_pages][Hkv][page_rows][D] bf16  page pool of the committed rows
  *   block_table [B][L_cap / page_rows] int32   logical rows [i P, (i+1) P) of
  *                                               sequence b live in page
@@ -225,7 +225,7 @@ MEDUSA_API int medusa_tree_attention_paged(const medusa_cfg* cfg, const void* Q,
                                 const void* Kt, const void* Vt, const int32_t* L, const uint64_t* anc_bits,
                                 void* O, void* workspace, medusa_stream_t stream);
 
-/* Commit the accepted path into a paged cache, in every layer (NEXT f4).
+/* Commit the accepted path into a paged cache, in every layer.
  * For layer l < n_layers the pools are Kp + l * pool_layer_elems (elements of
  * the cfg's type; same for Vp) and the staged rows Kt + l * tree_layer_elems:
  * for r = 0..acc_b, logical row L_b + r of sequence b receives the staged row
@@ -262,6 +262,29 @@ MEDUSA_API int medusa_kv_commit_paged(const medusa_cfg* cfg, void* Kp, void* Vp,
 MEDUSA_API int medusa_tree_attention_noalloc(const medusa_cfg* cfg, const void* Q, const void* Kc, const void* Vc,
                                              const int32_t* L, const uint64_t* anc_bits, void* O,
                                              medusa_stream_t stream);
+
+/* Failure detection. Every spin-wait of the tcgen05 kernels (the heads GEMVs and
+ * tree attention: pipeline mbarriers, the softmax exchanges) is bounded by a
+ * clock budget of about two seconds. On expiry the waiting thread ORs a code
+ * naming the wait into a device word of its kernel family, leaves its loop, and
+ * the kernel returns; the GPU context stays usable, but that call's outputs are
+ * invalid. The acceptance walks report the same per sequence in `flags`
+ * (MEDUSA_FLAG_TIMEOUT).
+ * medusa_poll_errors reads and clears both words, in stream order, and then
+ * synchronises `stream`. Returns MEDUSA_OK when no wait expired since the last
+ * poll, MEDUSA_ERR_TIMEOUT when one did (the codes, if the pointers are not
+ * NULL, receive the words' values: host pointers), MEDUSA_ERR_CUDA on a CUDA
+ * error. Not capturable in a CUDA graph (it synchronises). */
+MEDUSA_API int medusa_poll_errors(medusa_stream_t stream, uint32_t* heads_codes, uint32_t* attention_codes);
+
+/* Self-test of that path: enqueues one kernel whose single thread waits on an
+ * mbarrier that nothing completes, bounded by about `budget_us` microseconds
+ * (1 .. 1000000; MEDUSA_ERR_INVALID_ARG otherwise). It faults nothing and hangs
+ * nothing: after the budget it records MEDUSA_WAIT_SELFTEST_CODE in the
+ * attention word and returns, so the next medusa_poll_errors returns
+ * MEDUSA_ERR_TIMEOUT with that bit set in *attention_codes. */
+#define MEDUSA_WAIT_SELFTEST_CODE 0x80000000u
+MEDUSA_API int medusa_selftest_wait_timeout(uint32_t budget_us, medusa_stream_t stream);
 
 /* Number of kernels this library has enqueued in this process so far (host-side
  * counter, for diagnostics; no counterpart on the pages). */

@@ -21,8 +21,8 @@ FLAG_RS_NEAR_TIE, FLAG_CDF_NEAR_TIE, FLAG_CAPACITY = 1, 2, 4
 
 ENTRY_POINTS = ("medusa_node_count", "medusa_workspace_size", "medusa_heads", "medusa_tree_build",
                 "medusa_tree_attention", "medusa_verify", "medusa_kv_compact", "medusa_tree_attention_noalloc",
-                "medusa_tree_attention_paged", "medusa_kv_commit_paged", "medusa_launch_count",
-                "medusa_status_string")
+                "medusa_tree_attention_paged", "medusa_kv_commit_paged", "medusa_poll_errors",
+                "medusa_selftest_wait_timeout", "medusa_launch_count", "medusa_status_string")
 
 
 class MedusaError(RuntimeError):
@@ -84,6 +84,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                    ctypes.c_size_t, P, P, P, P, P],
         "medusa_verify": [cp, P, P, P, P, P, P, P, P, P, P, P, P, P, P],
         "medusa_kv_compact": [cp, P, P, P, P, P, P, P],
+        "medusa_poll_errors": [P, ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)],
+        "medusa_selftest_wait_timeout": [ctypes.c_uint32, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -121,6 +123,26 @@ def _check(name: str, status: int) -> None:
 
 def status_string(status: int) -> str:
     return load().medusa_status_string(status).decode()
+
+
+WAIT_SELFTEST_CODE = 0x80000000
+STATUS_TIMEOUT = -5
+
+
+def poll_errors(stream=None):
+    """Read and clear the device words that record expired bounded waits (synchronises the stream).
+
+    Returns (status, heads_codes, attention_codes); status is 0 or -5 (a wait expired)."""
+    h, a = ctypes.c_uint32(), ctypes.c_uint32()
+    s = load().medusa_poll_errors(_stream(stream), ctypes.byref(h), ctypes.byref(a))
+    if s not in (0, STATUS_TIMEOUT):
+        _check("medusa_poll_errors", s)
+    return s, int(h.value), int(a.value)
+
+
+def selftest_wait_timeout(budget_us: int, stream=None) -> None:
+    """Enqueue one bounded wait that nothing completes; the next poll_errors reports it."""
+    _check("medusa_selftest_wait_timeout", load().medusa_selftest_wait_timeout(int(budget_us), _stream(stream)))
 
 
 def launch_count() -> int:

@@ -204,6 +204,23 @@ int medusa_kv_commit_paged(const medusa_cfg* cfg, void* Kp, void* Vp, int32_t pa
                                           kv_map, (cudaStream_t)stream));
 }
 
+int medusa_poll_errors(medusa_stream_t stream, uint32_t* heads_codes, uint32_t* attention_codes) {
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t h = 0, a = 0;
+  cudaError_t e = heads_tc_take_error(&h, st);
+  if (e == cudaSuccess) e = attention_tc_take_error(&a, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return MEDUSA_ERR_CUDA;
+  if (heads_codes) *heads_codes = h;
+  if (attention_codes) *attention_codes = a;
+  return (h | a) ? MEDUSA_ERR_TIMEOUT : MEDUSA_OK;
+}
+
+int medusa_selftest_wait_timeout(uint32_t budget_us, medusa_stream_t stream) {
+  if (budget_us < 1 || budget_us > 1000000) return MEDUSA_ERR_INVALID_ARG;
+  return from_cuda(launch_wait_selftest((long long)budget_us * 2100, (cudaStream_t)stream));   // <= 2.1 GHz SM clock
+}
+
 uint64_t medusa_launch_count(void) { return (uint64_t)g_launches.load(std::memory_order_relaxed); }
 
 const char* medusa_status_string(int status) {

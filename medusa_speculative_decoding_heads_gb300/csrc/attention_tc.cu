@@ -749,6 +749,19 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   }
 }
 
+// A wait on an mbarrier that no thread or copy ever completes, bounded like every
+// wait of the kernels above: it exercises the expiry path (record a code, return)
+// without faulting or hanging the GPU.
+__global__ void wait_selftest_kernel(long long cycles) {
+  __shared__ __align__(8) uint64_t never;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&never, 1);
+    tc::mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) tc::mbar_wait<true>(&never, 0, &g_attention_tc_error, kWaitSelfTestCode, cycles);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
@@ -775,6 +788,20 @@ bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint
 }
 
 // Q-tile CTAs per (sequence, KV head): a short remainder rides with the last full tile.
+cudaError_t attention_tc_take_error(uint32_t* out, cudaStream_t st) {
+  static const uint32_t zero = 0;
+  cudaError_t e =
+      cudaMemcpyFromSymbolAsync(out, g_attention_tc_error, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbolAsync(g_attention_tc_error, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, st);
+}
+
+cudaError_t launch_wait_selftest(long long cycles, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(cycles);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
 int attention_tc_mtiles(int NG) { return NG / kRows + ((NG % kRows != 0 && extra_rows(NG) == 0) ? 1 : 0); }
 int attention_tc_ctas_x(int NG) { return attention_tc_mtiles(NG); }
 

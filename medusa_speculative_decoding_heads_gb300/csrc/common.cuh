@@ -137,6 +137,14 @@ cudaError_t launch_kv_commit_paged(const medusa_cfg& c, void* Kp, void* Vp, cons
                                    size_t pool_layer_elems, size_t tree_layer_elems, int32_t* L, const int32_t* acc,
                                    const int32_t* path, int32_t* kv_map, cudaStream_t st);
 size_t attention_workspace(const medusa_cfg& c);
+// Read-and-clear of the device words in which the tcgen05 kernels record expired waits
+// (stream-ordered; the caller synchronises before reading *out).
+cudaError_t heads_tc_take_error(uint32_t* out, cudaStream_t st);
+cudaError_t attention_tc_take_error(uint32_t* out, cudaStream_t st);
+// One bounded mbarrier wait that nothing completes: records kWaitSelfTestCode in the
+// attention kernels' error word after about `cycles` SM clocks.
+constexpr uint32_t kWaitSelfTestCode = 0x80000000u;
+cudaError_t launch_wait_selftest(long long cycles, cudaStream_t st);
 int attention_mma_warps(int NG, int* row_blocks);
 int attention_tc_mtiles(int NG);
 int attention_tc_ctas_x(int NG);

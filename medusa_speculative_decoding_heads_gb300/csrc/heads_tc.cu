@@ -376,6 +376,13 @@ HeadsTcPlan plan_heads_tc(const medusa_cfg& c) {
   return p;
 }
 
+cudaError_t heads_tc_take_error(uint32_t* out, cudaStream_t st) {
+  static const uint32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_heads_tc_error, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbolAsync(g_heads_tc_error, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, st);
+}
+
 bool heads_tc_supported(const medusa_cfg& c) { return c.dtype == MEDUSA_BF16 && c.B <= 32 && c.d % 64 == 0; }
 
 cudaError_t launch_heads_tc(const medusa_cfg& c, const void* h, const void* W, const void* bias, const void* U,

@@ -35,6 +35,13 @@ Readings where the pages are silent (each one repeated where it is used):
       inverse-CDF sampling picks the smallest y with cdf(y) > u * total.
   R11 compaction moves the accepted path's rows to the front of the tree
       region and advances the committed length by acc + 1.
+  R13 a pruned tree is the prefix-closed set of its nodes' rank paths; R2's
+      order and R3's tokens apply unchanged, and a leaf above depth K ends the
+      walk there (the bonus comes from that leaf's target row).
+  R14 a shared vocab projection is one matrix U [V][d] used by every head.
+  R15 a paged cache is a storage layout of the same logical cache: logical row
+      i of sequence b sits at offset i % P of page block_table[b][i // P]; the
+      tree's own rows are staged apart and follow the committed prefix.
 
 Parity status: every function below is pinned by tests under tests/ (closed
 forms, brute force, library routines, the pages' worked examples) except the
@@ -476,7 +483,7 @@ def kv_compact(Kc: np.ndarray, Vc: np.ndarray, L: np.ndarray, acc: np.ndarray, p
     return Kc, Vc, L_new, kv_map
 
 
-# --------------------------------------------------------------------------- paged cache (NEXT f4)
+# --------------------------------------------------------------------------- paged cache (R15)
 def paged_rows(pool: np.ndarray, block_table: np.ndarray, b: int, rows: int, page_rows: int) -> np.ndarray:
     """Logical rows [0, rows) of sequence b from a paged pool, [Hkv][rows][D].
 

@@ -416,7 +416,7 @@ def test_kv_compact_bit_exact(name):
     assert np.array_equal(i64(Ld), Lr) and np.array_equal(i64(st.kv_map), kv_map)
 
 
-# --------------------------------------------------------------------------- paged cache (NEXT f4)
+# --------------------------------------------------------------------------- paged cache
 def paged_layout(si, w, P, seed):
     """The committed rows of si.Kc/Vc moved into a shuffled page pool, the tree rows staged."""
     rng = np.random.default_rng(seed)
