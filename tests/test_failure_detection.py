@@ -32,6 +32,6 @@ def test_expired_wait_is_reported_once_and_the_context_stays_usable():
     # a whole step afterwards runs and checks out against the oracle, and leaves no error behind
     import test_gpu_parity as parity
     w = configs.scaled(configs.get("gqa7b_b32"), B=4, d=512, V=1000, Hq=8, Hkv=2, L_range=(40, 300),
-                       modes=(GREEDY,))
+                       modes=(GREEDY,), target_corr=0.0)
     parity.check_step(w, torch.device("cuda"))
     assert mb.poll_errors() == (0, 0, 0)
