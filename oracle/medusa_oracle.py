@@ -298,6 +298,32 @@ def tree_attention(Q: np.ndarray, Kc: np.ndarray, Vc: np.ndarray, L: np.ndarray,
     return O
 
 
+def attention_block_partial(q: np.ndarray, keys: np.ndarray, vals: np.ndarray, visible: np.ndarray):
+    """One key block's partial result for one query row, in the block-wise form of
+    [OPT-2] section 3.3 (attention over key blocks merged through the running
+    maximum and exp-sum): with s_j = q.k_j / sqrt(D) over the block's visible keys,
+    m = max_j s_j, l = sum_j exp(s_j - m), o = sum_j exp(s_j - m) v_j (not yet
+    divided by l). A block with no visible key gives (-inf, 0, 0)."""
+    D = q.shape[0]
+    s = (keys.astype(np.float64) @ q.astype(np.float64)) / math.sqrt(D)
+    s = s[visible.astype(bool)]
+    v = vals.astype(np.float64)[visible.astype(bool)]
+    if s.size == 0:
+        return -np.inf, 0.0, np.zeros(vals.shape[1])
+    m = float(s.max())
+    p = np.exp(s - m)
+    return m, float(p.sum()), p @ v
+
+
+def merge_attention_partials(parts) -> np.ndarray:
+    """Exact merge of block partials (m_i, l_i, o_i) ([OPT-2] section 3.3):
+    M = max_i m_i, l = sum_i exp(m_i - M) l_i, output = sum_i exp(m_i - M) o_i / l."""
+    M = max(m for m, _, _ in parts)
+    l = sum(math.exp(m - M) * li for m, li, _ in parts if m != -np.inf)
+    o = sum(math.exp(m - M) * oi for m, _, oi in parts if m != -np.inf)
+    return o / l
+
+
 # --------------------------------------------------------------------------- acceptance
 def children_of(parent: np.ndarray, node: int) -> List[int]:
     """Children in node-id order, which is rank order (R2)."""

@@ -104,3 +104,39 @@ def test_branches_do_not_interfere():
     for i in range(N):
         changed = not np.allclose(base[0, i], alt[0, i])
         assert changed == bool(mask[i, j])
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_block_partials_merge_to_the_one_pass_result(seed):
+    """Attention over key blocks merged by running max and exp-sum equals one softmax over all
+    keys (float64 SDPA), for random block sizes, an empty block and a block whose keys are all
+    masked; the order of the blocks does not matter."""
+    rng = np.random.default_rng(seed)
+    D, T = 16, 300
+    q = rng.standard_normal(D)
+    keys = 3.0 * rng.standard_normal((T, D))
+    vals = rng.standard_normal((T, D))
+    visible = rng.random(T) < 0.8
+    visible[200:230] = False                       # a fully masked block below
+    cuts = sorted(set([0, 17, 17, 128, 200, 230, 256, T]))
+    parts = [O.attention_block_partial(q, keys[a:b], vals[a:b], visible[a:b]) for a, b in zip(cuts[:-1], cuts[1:])]
+    parts.append(O.attention_block_partial(q, keys[:0], vals[:0], visible[:0]))   # an empty block
+    ref = F.scaled_dot_product_attention(torch.from_numpy(q)[None, None], torch.from_numpy(keys)[None],
+                                         torch.from_numpy(vals)[None],
+                                         attn_mask=torch.from_numpy(visible)[None, None])[0, 0].numpy()
+    np.testing.assert_allclose(O.merge_attention_partials(parts), ref, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(O.merge_attention_partials(parts[::-1]), ref, rtol=1e-12, atol=1e-13)
+
+
+def test_two_one_key_blocks_closed_form():
+    """Blocks holding one key each merge to the two-key softmax weights e^{s_i} / (e^{s_0} + e^{s_1})."""
+    D = 4
+    q = np.array([1.0, 0, 0, 0])
+    k0, k1 = np.array([[3.0, 0, 0, 0]]), np.array([[-1.0, 0, 0, 0]])
+    v0, v1 = np.array([[1.0, 0, 0, 0]]), np.array([[0, 1.0, 0, 0]])
+    one = np.ones(1, dtype=bool)
+    out = O.merge_attention_partials([O.attention_block_partial(q, k0, v0, one),
+                                      O.attention_block_partial(q, k1, v1, one)])
+    s0, s1 = 3.0 / math.sqrt(D), -1.0 / math.sqrt(D)
+    w0 = math.exp(s0) / (math.exp(s0) + math.exp(s1))
+    np.testing.assert_allclose(out, [w0, 1 - w0, 0, 0], rtol=1e-14)
