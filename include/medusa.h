@@ -26,7 +26,8 @@
  *     scratch comes from a caller-provided workspace of medusa_workspace_size()
  *     bytes (256-byte aligned).
  *   - Calls only enqueue work on `stream` (a cudaStream_t; NULL = legacy
- *     default stream) and never synchronize.
+ *     default stream) and never synchronize (except medusa_poll_errors, which
+ *     reads back the device's expired-wait words).
  *   - Return MEDUSA_OK (0) or a negative MEDUSA_ERR_*; on error nothing is
  *     enqueued. Device-side data errors never trap: they set bits in a
  *     per-sequence `flags` word and the affected sequence is skipped.
