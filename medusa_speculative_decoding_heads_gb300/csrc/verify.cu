@@ -957,10 +957,11 @@ cudaError_t launch_rs_walk(const medusa_cfg& c, const TreeShape& ts, int ncta, i
 }
 
 // CTAs per sequence: the largest power of two (at most 8) that keeps the whole
-// grid within two (256-thread) CTAs per SM.
+// grid within one CTA per SM (eight per sequence at B = 32 measured no faster
+// than four: the walk's time is its chain of cluster exchanges, not the slices).
 int rs_cluster_ctas(int B) {
   int n = 1;
-  while (n < kMaxCluster && (long)B * n * 2 <= 2 * 152) n *= 2;
+  while (n < kMaxCluster && (long)B * n <= 152) n *= 2;
   return n;
 }
 
