@@ -209,6 +209,34 @@ MEDUSA_API int medusa_verify(const medusa_cfg* cfg, const int32_t* tokens, const
 MEDUSA_API int medusa_kv_compact(const medusa_cfg* cfg, void* Kc, void* Vc, int32_t* L, const int32_t* acc,
                       const int32_t* path, int32_t* kv_map, medusa_stream_t stream);
 
+/* The whole step as one launch. medusa_step_graph_create captures the five
+ * calls above, in order, on a private stream into a CUDA graph (the kernels keep
+ * their programmatic-dependent-launch edges) and instantiates it;
+ * medusa_step_graph_launch then enqueues the step on `stream` with a single
+ * launch. The graph holds the pointers in `args`: every later launch reads the
+ * inputs from, and writes the outputs to, the same buffers, so a caller writes
+ * each step's inputs there (any lengths L within cfg->L_cap; the plan depends on
+ * the configuration only). Each call's checks run during creation: the first
+ * failing one's status is returned and nothing is kept. Creation and destruction
+ * use host memory and the driver's graph objects; they synchronise nothing but
+ * the private stream. Fields as in the calls above; head_logits for
+ * medusa_verify is `logits`; kv_compact = 0 leaves out step 5. */
+typedef struct {
+  const void* h; const void* W; const void* bias; const void* U; float* logits; int32_t* topk;
+  const int32_t* root_token; int32_t* L; int32_t* parent; int32_t* depth; int32_t* first_child;
+  uint8_t* mask; uint64_t* anc_bits; int32_t* tokens; int32_t* pos; uint32_t* flags;
+  const void* Q; void* Kc; void* Vc; void* O;
+  const void* target_logits; const float* u_acc; const float* u_res;
+  int32_t* acc; int32_t* path; int32_t* out_tokens; int32_t* n_out; int32_t* kv_map;
+  void* workspace;
+  int32_t kv_compact;
+} medusa_step_args;
+typedef struct medusa_step_graph medusa_step_graph;   /* opaque */
+MEDUSA_API int medusa_step_graph_create(const medusa_cfg* cfg, const medusa_step_args* args,
+                                        medusa_step_graph** graph);
+MEDUSA_API int medusa_step_graph_launch(medusa_step_graph* graph, medusa_stream_t stream);
+MEDUSA_API int medusa_step_graph_destroy(medusa_step_graph* graph);
+
 /* Tree attention over a paged KV cache. A page pool is read as a storage
  * layout of the same logical cache that medusa_tree_attention takes.
  *   Kp, Vp [num_pages][Hkv][page_rows][D] bf16  page pool of the committed rows

@@ -21,7 +21,8 @@ FLAG_RS_NEAR_TIE, FLAG_CDF_NEAR_TIE, FLAG_CAPACITY = 1, 2, 4
 
 ENTRY_POINTS = ("medusa_node_count", "medusa_workspace_size", "medusa_heads", "medusa_tree_build",
                 "medusa_tree_attention", "medusa_verify", "medusa_kv_compact", "medusa_tree_attention_noalloc",
-                "medusa_tree_attention_paged", "medusa_kv_commit_paged", "medusa_poll_errors",
+                "medusa_tree_attention_paged", "medusa_kv_commit_paged", "medusa_step_graph_create",
+                "medusa_step_graph_launch", "medusa_step_graph_destroy", "medusa_poll_errors",
                 "medusa_selftest_wait_timeout", "medusa_launch_count", "medusa_status_string")
 
 
@@ -59,6 +60,14 @@ def make_cfg(B: int, d: int, V: int, branching: Sequence[int], Hq: int, Hkv: int
     return c
 
 
+class StepArgs(ctypes.Structure):
+    """medusa_step_args: every buffer of the five calls, in the header's order."""
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "h", "W", "bias", "U", "logits", "topk", "root_token", "L", "parent", "depth", "first_child", "mask",
+        "anc_bits", "tokens", "pos", "flags", "Q", "Kc", "Vc", "O", "target_logits", "u_acc", "u_res", "acc", "path",
+        "out_tokens", "n_out", "kv_map", "workspace")] + [("kv_compact", ctypes.c_int32)]
+
+
 _lib: Optional[ctypes.CDLL] = None
 P = ctypes.c_void_p
 
@@ -85,6 +94,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "medusa_verify": [cp, P, P, P, P, P, P, P, P, P, P, P, P, P, P],
         "medusa_kv_compact": [cp, P, P, P, P, P, P, P],
         "medusa_poll_errors": [P, ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)],
+        "medusa_step_graph_create": [cp, ctypes.POINTER(StepArgs), ctypes.POINTER(ctypes.c_void_p)],
+        "medusa_step_graph_launch": [P, P],
+        "medusa_step_graph_destroy": [P],
         "medusa_selftest_wait_timeout": [ctypes.c_uint32, P],
     }
     for name, args in sig.items():
@@ -123,6 +135,33 @@ def _check(name: str, status: int) -> None:
 
 def status_string(status: int) -> str:
     return load().medusa_status_string(status).decode()
+
+
+class StepGraph:
+    """The whole step captured once as a CUDA graph over fixed buffers, replayed with one launch."""
+
+    def __init__(self, cfg: "Cfg", **buffers):
+        args = StepArgs(**{k: _ptr(v) for k, v in buffers.items() if k != "kv_compact"},
+                        kv_compact=int(bool(buffers.get("kv_compact", 1))))
+        self._cfg, self._args = cfg, args   # kept alive with the graph
+        h = ctypes.c_void_p()
+        _check("medusa_step_graph_create", load().medusa_step_graph_create(ctypes.byref(cfg), ctypes.byref(args),
+                                                                            ctypes.byref(h)))
+        self._h = h
+
+    def launch(self, stream=None) -> None:
+        _check("medusa_step_graph_launch", load().medusa_step_graph_launch(self._h, _stream(stream)))
+
+    def close(self) -> None:
+        if self._h is not None and self._h.value:
+            _check("medusa_step_graph_destroy", load().medusa_step_graph_destroy(self._h))
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 WAIT_SELFTEST_CODE = 0x80000000

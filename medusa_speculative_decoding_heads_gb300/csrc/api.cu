@@ -204,6 +204,75 @@ int medusa_kv_commit_paged(const medusa_cfg* cfg, void* Kp, void* Vp, int32_t pa
                                           kv_map, (cudaStream_t)stream));
 }
 
+}  // extern "C"
+
+struct medusa_step_graph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  unsigned long long kernels = 0;   // kernel launches one replay stands for
+};
+
+extern "C" {
+
+int medusa_step_graph_create(const medusa_cfg* cfg, const medusa_step_args* a, medusa_step_graph** out) {
+  if (!cfg || !a || !out) return MEDUSA_ERR_INVALID_ARG;
+  *out = nullptr;
+  int status = check_cfg(cfg);
+  if (status != MEDUSA_OK) return status;
+  cudaStream_t st = nullptr;
+  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaStreamDestroy(st);
+    return MEDUSA_ERR_CUDA;
+  }
+  const unsigned long long before = g_launches.load(std::memory_order_relaxed);
+  const medusa_stream_t ms = (medusa_stream_t)st;
+  status = medusa_heads(cfg, a->h, a->W, a->bias, a->U, a->logits, a->topk, a->workspace, ms);
+  if (status == MEDUSA_OK)
+    status = medusa_tree_build(cfg, a->root_token, a->topk, a->L, a->parent, a->depth, a->first_child, a->mask,
+                               a->anc_bits, a->tokens, a->pos, a->flags, ms);
+  if (status == MEDUSA_OK)
+    status = medusa_tree_attention(cfg, a->Q, a->Kc, a->Vc, a->L, a->anc_bits, a->O, a->workspace, ms);
+  if (status == MEDUSA_OK)
+    status = medusa_verify(cfg, a->tokens, a->parent, a->first_child, a->target_logits, a->logits, a->u_acc, a->u_res,
+                           a->acc, a->path, a->out_tokens, a->n_out, a->flags, a->workspace, ms);
+  if (status == MEDUSA_OK && a->kv_compact)
+    status = medusa_kv_compact(cfg, a->Kc, a->Vc, a->L, a->acc, a->path, a->kv_map, ms);
+  const unsigned long long kernels = g_launches.load(std::memory_order_relaxed) - before;
+  g_launches.fetch_sub(kernels, std::memory_order_relaxed);   // captured, not launched
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ended = cudaStreamEndCapture(st, &graph);   // ends the capture on every path
+  cudaStreamDestroy(st);
+  if (status == MEDUSA_OK && (ended != cudaSuccess || !graph)) status = MEDUSA_ERR_CUDA;
+  cudaGraphExec_t exec = nullptr;
+  if (status == MEDUSA_OK && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) status = MEDUSA_ERR_CUDA;
+  if (status != MEDUSA_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();   // a failed call inside the capture leaves no sticky error behind
+    return status;
+  }
+  medusa_step_graph* g = new medusa_step_graph;
+  g->graph = graph;
+  g->exec = exec;
+  g->kernels = kernels;
+  *out = g;
+  return MEDUSA_OK;
+}
+
+int medusa_step_graph_launch(medusa_step_graph* g, medusa_stream_t stream) {
+  if (!g) return MEDUSA_ERR_INVALID_ARG;
+  if (cudaGraphLaunch(g->exec, (cudaStream_t)stream) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  g_launches.fetch_add(g->kernels, std::memory_order_relaxed);
+  return MEDUSA_OK;
+}
+
+int medusa_step_graph_destroy(medusa_step_graph* g) {
+  if (!g) return MEDUSA_ERR_INVALID_ARG;
+  const bool ok = cudaGraphExecDestroy(g->exec) == cudaSuccess && cudaGraphDestroy(g->graph) == cudaSuccess;
+  delete g;
+  return ok ? MEDUSA_OK : MEDUSA_ERR_CUDA;
+}
+
 int medusa_poll_errors(medusa_stream_t stream, uint32_t* heads_codes, uint32_t* attention_codes) {
   cudaStream_t st = (cudaStream_t)stream;
   uint32_t h = 0, a = 0;

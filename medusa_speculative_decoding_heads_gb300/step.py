@@ -2,9 +2,10 @@
 
 ``DeviceStep`` owns the device buffers of one workload (inputs, outputs and the
 library workspace) and enqueues the five library calls in order on one
-stream: heads -> tree build -> tree attention -> verify -> KV compaction. It
-only allocates tensors and marshals pointers; all arithmetic runs in
-libmedusa's kernels.
+stream: heads -> tree build -> tree attention -> verify -> KV compaction, or
+captures them once as a library step graph replayed with one launch. It only
+allocates tensors and marshals pointers; all arithmetic runs in libmedusa's
+kernels.
 """
 from __future__ import annotations
 
@@ -87,6 +88,21 @@ class DeviceStep:
         self.verify(inp.target_logits, inp.u_acc, inp.u_res)
         if compact:
             self.kv_compact(inp.Kc, inp.Vc, inp.L)
+
+
+    def graph(self, inp: "DeviceInputs", write_logits: bool = False, compact: bool = True) -> mb.StepGraph:
+        """The same five calls captured once as a CUDA graph over these buffers (one launch per step)."""
+        rs = self.mode == REJECTION
+        if self.O is None or self.O.shape != inp.Q.shape:
+            self.O = torch.empty_like(inp.Q)
+        return mb.StepGraph(
+            self.cfg, h=inp.h, W=inp.W, bias=inp.bias, U=inp.U,
+            logits=self.logits if (write_logits or rs) else None, topk=self.topk, root_token=inp.root_token,
+            L=inp.L, parent=self.parent, depth=self.depth, first_child=self.first_child, mask=self.mask,
+            anc_bits=self.anc_bits, tokens=self.tokens, pos=self.pos, flags=self.flags, Q=inp.Q, Kc=inp.Kc,
+            Vc=inp.Vc, O=self.O, target_logits=inp.target_logits, u_acc=inp.u_acc if rs else None,
+            u_res=inp.u_res if rs else None, acc=self.acc, path=self.path, out_tokens=self.out_tokens,
+            n_out=self.n_out, kv_map=self.kv_map, workspace=self.workspace, kv_compact=compact)
 
 
 @dataclass
