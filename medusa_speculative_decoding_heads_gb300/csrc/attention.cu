@@ -31,7 +31,7 @@ constexpr int kKeyTile = 32;
 
 struct AttnPlan {
   int G, NG, row_groups, nsplit, chunk;
-  size_t o_part, ml_part, total;
+  size_t o_part, ml_part, x_part, total;
 };
 
 // Kernel choice: float32 -> CUDA cores; bf16 with D = 128 -> tcgen05; bf16 with D = 64 -> mma.sync.
@@ -75,6 +75,8 @@ AttnPlan plan_attention(const medusa_cfg& c) {
   off = align_up(off + rows * c.D * 4, 256);
   p.ml_part = off;
   off = align_up(off + rows * 2 * 4, 256);
+  p.x_part = off;   // leftover rows' partials (tcgen05 path with a short remainder of query rows)
+  off = align_up(off + (path == kPathTc ? attention_tc_xpart_bytes(c, p.nsplit) : 0), 256);
   p.total = off;
   return p;
 }
@@ -246,9 +248,11 @@ cudaError_t run(const medusa_cfg& c, const AttnPlan& p, const void* Q, const voi
   float* ml_part = reinterpret_cast<float*>(ws + p.ml_part);
   cudaError_t e;
   const int path = attention_path(c);
+  float* x_part = reinterpret_cast<float*>(ws + p.x_part);
   if (path == kPathTc) {
-    e = launch_attention_tc(c, p.nsplit, p.chunk, Q, Kc, Vc, L, bits, o_part, ml_part, O, st, paged);
-    if (e != cudaSuccess || p.nsplit == 1) return e;   // a single split writes O itself
+    e = launch_attention_tc(c, p.nsplit, p.chunk, Q, Kc, Vc, L, bits, o_part, ml_part, x_part, O, st, paged);
+    if (e == cudaSuccess && p.nsplit == 1) e = launch_attention_tc_xmerge(c, 1, x_part, L, O, st);
+    if (e != cudaSuccess || p.nsplit == 1) return e;   // a single split writes O itself (leftover rows merged)
   } else if (path == kPathMma) {
     e = launch_attention_mma(c, p.nsplit, p.chunk, Q, Kc, Vc, L, bits, o_part, ml_part, st);
   } else {
@@ -265,7 +269,9 @@ cudaError_t run(const medusa_cfg& c, const AttnPlan& p, const void* Q, const voi
   launch_pdl(tree_attn_merge_kernel<T, D>, (unsigned)((rows * 32 + 255) / 256), 256, 0, st, 
       o_part, ml_part, c.B, ts.N, c.Hq, p.nsplit, L, c.L_cap, static_cast<T*>(O));
   note_launches(1);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess && path == kPathTc) e = launch_attention_tc_xmerge(c, p.nsplit, x_part, L, O, st);
+  return e;
 }
 
 }  // namespace

@@ -170,7 +170,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     const uint16_t* __restrict__ Q, const int32_t* __restrict__ L, const uint64_t* __restrict__ bits,
                     int N, int Hq, int Hkv, int L_cap, int chunk, float scale_log2, float* __restrict__ o_part,
                     float* __restrict__ ml_part, uint16_t* __restrict__ O, const int32_t* __restrict__ block_table,
-                    int page_rows) {
+                    int page_rows, float* __restrict__ x_part) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
@@ -205,11 +205,17 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = Hq / Hkv, NG = N * G;
-  const int R = (kFold && mt == (int)gridDim.x - 1) ? extra_rows(NG) : 0;   // leftover rows this CTA carries
+  // Leftover rows: every Q-tile CTA of the KV head carries them on its share of the key tiles
+  // (tiles j with j % MT == mt), so that the CTAs that share each K/V tile through L2 keep the
+  // same pace; their partial results merge in tree_attn_xmerge_kernel.
+  const int MT = (int)gridDim.x;
+  const int R = kFold ? extra_rows(NG) : 0;
   const bool xtra = R > 0;
   const bool xs = xtra && warp >= kXWarp0 && warp < kXWarp0 + 4;   // a leftover-row softmax thread
   const int xt = 32 * (warp & 3) + lane;     // its TMEM lane: key of S'^T, head dim of O'^T
-  const int xq0 = kRows * (mt + 1);          // query row index of leftover row 0
+  const int xq0 = kRows * MT;                // query row index of leftover row 0
+  // this CTA's leftover partial (o[D], m, l) of row r: x_part + (xbase + r) * (kD + 2)
+  const size_t xbase = ((((size_t)b * Hkv + kvh) * nsplit + split) * MT + mt) * kXMax;
   const int Lb = L[b];
   const bool valid = Lb >= 0 && Lb + N <= L_cap;
   const int k_begin = split * chunk;
@@ -241,18 +247,17 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         ml_part[2 * orow + 1] = 0.f;
       }
     }
-    if (xs) {
-      for (int r = 0; r < R; ++r) {
-        const int xqi = xq0 + r, xnode = xqi / G, xqh = kvh * G + xqi % G;
-        const size_t orow = (((size_t)b * nsplit + split) * N + xnode) * Hq + xqh;
-        if (nsplit == 1) {
-          O[(((size_t)b * N + xnode) * Hq + xqh) * kD + xt] = 0;
-        } else if (xt == 0) {
+    if (xs && xt == 0)
+      for (int r = 0; r < R; ++r) {   // an empty leftover partial
+        x_part[(xbase + r) * (kD + 2) + kD] = -INFINITY;
+        x_part[(xbase + r) * (kD + 2) + kD + 1] = 0.f;
+        if (nsplit > 1 && mt == 0) {   // the split merge leaves these rows empty; the leftover merge fills them
+          const int xqi = xq0 + r;
+          const size_t orow = (((size_t)b * nsplit + split) * N + xqi / G) * Hq + kvh * G + xqi % G;
           ml_part[2 * orow] = -INFINITY;
           ml_part[2 * orow + 1] = 0.f;
         }
       }
-    }
     return;
   }
 
@@ -401,10 +406,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         tc::commit(&s_full[slot]);
       }
       __syncwarp();
-      if (xtra) {
-        // S'^T_j = K_j Q'^T, once PV'_{j-2} completed: its softmax had read S' slot j & 1, and
-        // P' slot j & 1 is free for the softmax of tile j
-        if (j >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait<true>(&p2_free[slot], ((j >> 1) - 1) & 1, err, 1024)))
+      if (xtra && j % MT == mt) {
+        // S'^T = K_j Q'^T for this CTA's narrow tile jx, once PV'_{jx-2} completed: its softmax
+        // had read S' slot jx & 1, and P' slot jx & 1 is free for the softmax of tile jx
+        const int jx = j / MT, sx = jx & 1;
+        if (jx >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait<true>(&p2_free[sx], ((jx >> 1) - 1) & 1, err, 1024)))
           break;
         tc::fence_after();
         if (tc::elect_one()) {
@@ -413,9 +419,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
             const uint32_t offx = ((kk >> 2) * kXHalf + (kk & 3) * 32) >> 4;
-            tc::mma_bf16(tmem + kColS2 + 16 * slot, a0 + off, dQx + offx, idS2, kk > 0);
+            tc::mma_bf16(tmem + kColS2 + 16 * sx, a0 + off, dQx + offx, idS2, kk > 0);
           }
-          tc::commit(&s2_full[slot]);
+          tc::commit(&s2_full[sx]);
         }
         __syncwarp();
       }
@@ -428,19 +434,20 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     constexpr uint32_t idPV2 = tc::idesc_bf16_f32(kD, kXRows, 1, 0);   // A = V^T (MN-major), B = P' (K-major)
     const uint64_t dV = tc::sw128_desc(tc::saddr(ring + kOperand), kHalf, 1024);   // MN-major: LBO = 64-column half
     const uint64_t dPx = tc::sw128_desc(tc::saddr(sm + kOffPx), 16, 1024);
-    // O'^T += V_t^T P'_t^T once the leftover softmax of tile t has arrived; it also frees the stage
-    auto issue_pv2 = [&](int t) {
-      if (!__all_sync(0xffffffffu, tc::mbar_wait<true>(&p2_full[t & 1], (t >> 1) & 1, err, 2048))) return false;
+    // O'^T += V_t^T P'^T for narrow tile jx (key tile t) once its leftover softmax has arrived;
+    // its completion also frees the stage
+    auto issue_pv2 = [&](int t, int jx) {
+      if (!__all_sync(0xffffffffu, tc::mbar_wait<true>(&p2_full[jx & 1], (jx >> 1) & 1, err, 2048))) return false;
       tc::fence_after();
       if (tc::elect_one()) {
         const uint64_t a0 = dV + (uint64_t)(((t % kStages) * kStage) >> 4);
-        const uint64_t p0 = dPx + (uint64_t)(((t & 1) * 2 * kXHalf) >> 4);
+        const uint64_t p0 = dPx + (uint64_t)(((jx & 1) * 2 * kXHalf) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
           const uint32_t offx = ((kk >> 2) * kXHalf + (kk & 3) * 32) >> 4;
-          tc::mma_bf16(tmem + kColO2, a0 + (uint64_t)((kk * 2048) >> 4), p0 + offx, idPV2, (t > 0 || kk > 0) ? 1 : 0);
+          tc::mma_bf16(tmem + kColO2, a0 + (uint64_t)((kk * 2048) >> 4), p0 + offx, idPV2, (jx > 0 || kk > 0) ? 1 : 0);
         }
-        tc::commit(&p2_free[t & 1]);
+        tc::commit(&p2_free[jx & 1]);
         tc::commit(&kv_empty[t % kStages]);
       }
       __syncwarp();
@@ -458,10 +465,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           tc::mma_bf16_tmem_a(tmem + kColO, tmem + col_S(slot) + 32 * (kk >> 1) + 8 * (kk & 1),
                               b0 + (uint64_t)((kk * 2048) >> 4), idPV, (j > 0 || kk > 0) ? 1 : 0);
         tc::commit(&p_free[slot]);
-        if (!xtra) tc::commit(&kv_empty[st]);
+        if (!(xtra && j % MT == mt)) tc::commit(&kv_empty[st]);
       }
       __syncwarp();
-      if (xtra && !issue_pv2(j)) break;
+      if (xtra && j % MT == mt && !issue_pv2(j, j / MT)) break;
     }
   } else if (smx) {
     // ------------------------------------------------------------------ softmax
@@ -596,10 +603,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   } else if (xs) {
     // ------------------------------------------------------- leftover-row softmax
     // Thread xt holds key xt of S'^T (one score per leftover row) and head dim xt of
-    // O'^T. Row maxima: warp shuffles, then the four warps' values through shared
-    // memory (double-buffered by tile parity, one mbarrier phase per tile).
+    // O'^T. This CTA's narrow tiles are the key tiles j = jx * MT + mt. Row maxima: warp
+    // shuffles, then the four warps' values through shared memory (double-buffered by
+    // the narrow tile's parity, one mbarrier phase per narrow tile).
     const uint32_t xl_base = (uint32_t)(32 * (warp & 3)) << 16;
     float* red = reinterpret_cast<float*>(sm + kOffRed);   // maxima [parity][warp][row], then sums [warp][row]
+    const int nx = ntiles > mt ? (ntiles - 1 - mt) / MT + 1 : 0;
     float m_run[kXMax], l_t[kXMax], corr[kXMax];
 #pragma unroll
     for (int r = 0; r < kXMax; ++r) {
@@ -607,9 +616,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       l_t[r] = 0.f;
     }
     bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int slot = j & 1;
-      ok = tc::mbar_wait(&s2_full[slot], (j >> 1) & 1, err, 4096);
+    for (int jx = 0; jx < nx; ++jx) {
+      const int j = jx * MT + mt, slot = jx & 1;
+      ok = tc::mbar_wait(&s2_full[slot], (jx >> 1) & 1, err, 4096);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -638,7 +647,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         }
       }
       tc::mbar_arrive(&xbar2);
-      ok = tc::mbar_wait(&xbar2, j & 1, err, 8192);
+      ok = tc::mbar_wait(&xbar2, jx & 1, err, 8192);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -657,7 +666,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         }
       }
       // P' row r, key xt -> the B operand of O'^T += V^T P'^T ([row][key], K-major, 128-byte
-      // swizzle, two 64-key halves). Its slot last fed PV'_{j-2}, complete before S'_j.
+      // swizzle, two 64-key halves). Its slot last fed PV'_{jx-2}, complete before S'_jx.
       uint8_t* pr = sm + kOffPx + slot * 2 * kXHalf + (xt >> 6) * kXHalf;
       const int cc = xt & 63;
 #pragma unroll
@@ -670,9 +679,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           *reinterpret_cast<uint16_t*>(pr + r * 128 + ((((cc >> 3) ^ (r & 7)) << 4) | ((cc & 7) << 1))) = hv;
         }
       }
-      if (j >= 1 && any) {
-        // rescale O'^T once PV'_{j-1} has landed (thread = head dim, column = row)
-        ok = tc::mbar_wait(&p2_free[(j - 1) & 1], ((j - 1) >> 1) & 1, err, 16384);
+      if (jx >= 1 && any) {
+        // rescale O'^T once PV'_{jx-1} has landed (thread = head dim, column = row)
+        ok = tc::mbar_wait(&p2_free[(jx - 1) & 1], ((jx - 1) >> 1) & 1, err, 16384);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
@@ -690,8 +699,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       tc::fence_before();
       tc::mbar_arrive(&p2_full[slot]);
     }
-    if (ok) ok = tc::mbar_wait(&p2_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, err, 32768);
-    const bool have = __all_sync(0xffffffffu, ok);
+    if (ok && nx > 0) ok = tc::mbar_wait(&p2_free[(nx - 1) & 1], ((nx - 1) >> 1) & 1, err, 32768);
+    const bool have = __all_sync(0xffffffffu, ok) && nx > 0;
     tc::fence_after();
     // row sums over the 128 key lanes
     float* rs = red + 128;
@@ -705,7 +714,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       }
     }
     tc::mbar_arrive(&xbar2);
-    const bool summed = tc::mbar_wait(&xbar2, ntiles & 1, err, 65536);
+    const bool summed = tc::mbar_wait(&xbar2, nx & 1, err, 65536);
     uint32_t ov[kXMax];
     if (have) {   // warp-uniform: the TMEM load is a collective of the warp
       tc::tmem_ld8(tmem + kColO2 + xl_base, ov);
@@ -714,28 +723,22 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 #pragma unroll
       for (int r = 0; r < kXMax; ++r) ov[r] = 0u;
     }
-    for (int r = 0; r < R; ++r) {
-      const float l_tot = summed ? (rs[r] + rs[16 + r]) + (rs[32 + r] + rs[48 + r]) : 0.f;
-      const int xqi = xq0 + r, xnode = xqi / G, xqh = kvh * G + xqi % G;
-      float o = 0.f;
+    // this CTA's partial of every leftover row: unnormalised O', running max (log2) and exp-sum
 #pragma unroll
-      for (int u = 0; u < kXMax; ++u)
-        if (u == r) o = __uint_as_float(ov[u]);   // register arrays take compile-time indexes
-      if (nsplit == 1) {
-        const float inv = (have && l_tot > 0.f) ? 1.f / l_tot : 0.f;
-        uint16_t hv;
-        asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(hv) : "f"(o * inv));
-        O[(((size_t)b * N + xnode) * Hq + xqh) * kD + xt] = hv;
-      } else {
-        const size_t orow = (((size_t)b * nsplit + split) * N + xnode) * Hq + xqh;
-        o_part[orow * kD + xt] = o;
+    for (int r = 0; r < kXMax; ++r) {
+      if (r < R) {
+        float* xp = x_part + (xbase + r) * (kD + 2);
+        xp[xt] = __uint_as_float(ov[r]);
         if (xt == 0) {
-          float mr = -INFINITY;
-#pragma unroll
-          for (int u = 0; u < kXMax; ++u)
-            if (u == r) mr = m_run[u];
-          ml_part[2 * orow] = have ? mr : -INFINITY;
-          ml_part[2 * orow + 1] = have ? l_tot : 0.f;
+          const bool live = have && summed;
+          xp[kD] = live ? m_run[r] : -INFINITY;
+          xp[kD + 1] = live ? (rs[r] + rs[16 + r]) + (rs[32 + r] + rs[48 + r]) : 0.f;
+          if (nsplit > 1 && mt == 0) {   // the split merge leaves these rows empty; the leftover merge fills them
+            const int xqi = xq0 + r;
+            const size_t orow = (((size_t)b * nsplit + split) * N + xqi / G) * Hq + kvh * G + xqi % G;
+            ml_part[2 * orow] = -INFINITY;
+            ml_part[2 * orow + 1] = 0.f;
+          }
         }
       }
     }
@@ -760,6 +763,44 @@ __global__ void wait_selftest_kernel(long long cycles) {
   }
   __syncthreads();
   if (threadIdx.x == 0) tc::mbar_wait<true>(&never, 0, &g_attention_tc_error, kWaitSelfTestCode, cycles);
+}
+
+// Leftover rows: O = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c over the partials of the
+// MT Q-tile CTAs and the KV splits of its (sequence, KV head) (the running max / exp-sum
+// merge of "최적화 2편" section 3.3). One warp per leftover row; lane = 4 head dims.
+__global__ void __launch_bounds__(256)
+tree_attn_xmerge_kernel(const float* __restrict__ x_part, int B, int Hkv, int nsplit, int MT, int R, int N, int G,
+                        const int32_t* __restrict__ L, int L_cap, uint16_t* __restrict__ O) {
+  pdl_wait();
+  pdl_trigger();
+  const int row = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+  if (row >= B * Hkv * R) return;
+  const int r = row % R, kvh = (row / R) % Hkv, b = row / (R * Hkv);
+  const int Lb = L[b];
+  const bool valid = Lb >= 0 && Lb + N <= L_cap;
+  const int parts = nsplit * MT;
+  const float* p0 = x_part + ((size_t)(b * Hkv + kvh) * parts * kXMax + r) * (kD + 2);   // partial c at + c * kXMax
+  float M = -INFINITY;
+  for (int c = 0; c < parts; ++c) M = fmaxf(M, p0[(size_t)c * kXMax * (kD + 2) + kD]);
+  float l = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c = 0; c < parts; ++c) {
+    const float* pc = p0 + (size_t)c * kXMax * (kD + 2);
+    const float m = pc[kD];
+    if (m == -INFINITY) continue;   // an empty partial need not have written its O
+    const float w = exp2f(m - M);
+    l += w * pc[kD + 1];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] += w * pc[lane + 32 * e];
+  }
+  const int qi = kRows * MT + r, Hq = Hkv * G;
+  uint16_t* out = O + (((size_t)b * N + qi / G) * Hq + kvh * G + qi % G) * kD;
+  const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    uint16_t hv;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(hv) : "f"(o[e] * inv));
+    out[lane + 32 * e] = hv;
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -805,9 +846,28 @@ cudaError_t launch_wait_selftest(long long cycles, cudaStream_t st) {
 int attention_tc_mtiles(int NG) { return NG / kRows + ((NG % kRows != 0 && extra_rows(NG) == 0) ? 1 : 0); }
 int attention_tc_ctas_x(int NG) { return attention_tc_mtiles(NG); }
 
+// Workspace for the leftover rows' partials: (sequence, KV head, split, Q-tile CTA, row) x (D + 2) floats.
+size_t attention_tc_xpart_bytes(const medusa_cfg& c, int nsplit) {
+  const int NG = tree_shape(c).N * (c.Hq / c.Hkv);
+  if (c.dtype != MEDUSA_BF16 || c.D != kD || extra_rows(NG) == 0) return 0;
+  return (size_t)c.B * c.Hkv * nsplit * attention_tc_mtiles(NG) * kXMax * (kD + 2) * sizeof(float);
+}
+
+cudaError_t launch_attention_tc_xmerge(const medusa_cfg& c, int nsplit, const float* x_part, const int32_t* L, void* O,
+                                       cudaStream_t st) {
+  const TreeShape ts = tree_shape(c);
+  const int G = c.Hq / c.Hkv, NG = ts.N * G, R = extra_rows(NG);
+  if (R == 0) return cudaSuccess;
+  const int rows = c.B * c.Hkv * R;
+  launch_pdl(tree_attn_xmerge_kernel, (rows * 32 + 255) / 256, 256, 0, st, x_part, c.B, c.Hkv, nsplit,
+             attention_tc_mtiles(NG), R, ts.N, G, L, c.L_cap, static_cast<uint16_t*>(O));
+  note_launches(1);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, const void* Q, const void* Kc,
                                 const void* Vc, const int32_t* L, const uint64_t* bits, float* o_part, float* ml_part,
-                                void* O, cudaStream_t st, const PagedKV* paged) {
+                                float* x_part, void* O, cudaStream_t st, const PagedKV* paged) {
   const TreeShape ts = tree_shape(c);
   CUtensorMap tmK, tmV, tmKt, tmVt;
   if (paged) {   // pool [pages][Hkv][page_rows][D]; staged tree rows [B][Hkv][N][D]
@@ -834,7 +894,7 @@ cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, cons
   dim3 grid(attention_tc_mtiles(NG), c.Hkv * c.B, nsplit);
   launch_pdl(kernel, grid, threads_of(fold), smem_of(fold), st, tmK, tmV, tmKt, tmVt, static_cast<const uint16_t*>(Q),
              L, bits, ts.N, c.Hq, c.Hkv, c.L_cap, chunk, scale_log2, o_part, ml_part, static_cast<uint16_t*>(O),
-             paged ? paged->block_table : static_cast<const int32_t*>(nullptr), paged ? paged->page_rows : 0);
+             paged ? paged->block_table : static_cast<const int32_t*>(nullptr), paged ? paged->page_rows : 0, x_part);
   note_launches(1);
   return cudaGetLastError();
 }

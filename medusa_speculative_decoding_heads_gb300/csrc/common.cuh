@@ -150,7 +150,10 @@ int attention_tc_mtiles(int NG);
 int attention_tc_ctas_x(int NG);
 cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, const void* Q, const void* Kc,
                                 const void* Vc, const int32_t* L, const uint64_t* bits, float* o_part, float* ml_part,
-                                void* O, cudaStream_t st, const PagedKV* paged);
+                                float* x_part, void* O, cudaStream_t st, const PagedKV* paged);
+size_t attention_tc_xpart_bytes(const medusa_cfg& c, int nsplit);
+cudaError_t launch_attention_tc_xmerge(const medusa_cfg& c, int nsplit, const float* x_part, const int32_t* L, void* O,
+                                       cudaStream_t st);
 cudaError_t launch_attention_mma(const medusa_cfg& c, int nsplit, int chunk, const void* Q, const void* Kc,
                                  const void* Vc, const int32_t* L, const uint64_t* bits, float* o_part, float* ml_part,
                                  cudaStream_t st);
