@@ -40,7 +40,9 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per medusa_heads call, from the committed ncu capture of the heads
 # kernels on a reduced vocabulary (V=8000: traffic 1.02x the algorithmic
 # weight bytes), scaled to the workload's weight rows. Absent = not captured.
-NCU_TRAFFIC_BYTES = {"vicuna7b_b1": 1189250048, "vicuna7b_b1_shared": 402850048}   # dram read + write of the medusa_heads kernels, one call
+# dram read + write of the dominant call's kernels, one call (ncu captures summarised in profiles/)
+NCU_TRAFFIC_BYTES = {"vicuna7b_b1": 1189250048, "vicuna7b_b1_shared": 402850048, "vicuna13b_b8": 1918169600}   # medusa_heads
+NCU_ATTN_TRAFFIC_BYTES = {"gqa7b_b32": 1512225024}   # medusa_tree_attention
 
 
 def parse():
@@ -457,7 +459,7 @@ def run_ours(args):
     attn_ms = per_call["tree_attention"]
     if attn_ms > heads_ms:   # the dominant call is tree attention (long committed prefixes)
         kernel = "medusa_tree_attention (tcgen05 tree attention over the committed KV)"
-        dom_bytes, dom_ms, traffic = by["kv"] + by["tree_qkv"] + by["attn_out"], attn_ms, None
+        dom_bytes, dom_ms, traffic = by["kv"] + by["tree_qkv"] + by["attn_out"], attn_ms, NCU_ATTN_TRAFFIC_BYTES.get(w.name)
     else:
         kernel = "medusa_heads (residual + vocab projection GEMV, top-s)"
         dom_bytes, dom_ms, traffic = heads_bytes, heads_ms, NCU_TRAFFIC_BYTES.get(w.name)
