@@ -42,7 +42,7 @@ FALLBACK_HBM_GBS = 6800.0
 # weight bytes), scaled to the workload's weight rows. Absent = not captured.
 # dram read + write of the dominant call's kernels, one call (ncu captures summarised in profiles/)
 NCU_TRAFFIC_BYTES = {"vicuna7b_b1": 1189250048, "vicuna7b_b1_shared": 402850048, "vicuna13b_b8": 1918169600}   # medusa_heads
-NCU_ATTN_TRAFFIC_BYTES = {"gqa7b_b32": 1512225024}   # medusa_tree_attention
+NCU_ATTN_TRAFFIC_BYTES = {"gqa7b_b32": 1512225024, "vicuna33b_b16": 3573720576}   # medusa_tree_attention
 
 
 def parse():
