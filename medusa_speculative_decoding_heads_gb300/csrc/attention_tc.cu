@@ -21,12 +21,15 @@
 //           rescaled) only on a jump of more than 2^8.
 //   warps 19-22 leftover rows: when the query rows of a KV head end in a short
 //           remainder of at most 8 rows (4 rows for 65 nodes x 4 heads), the
-//           last full tile's CTA carries them instead of a CTA of its own, with
-//           transposed narrow products on the same K/V tiles: S'^T = K Q'^T
-//           (M = 128 keys, N = 16 rows) right behind S_j, and O'^T += V^T P'^T
-//           (M = 128 head dims) right behind PV_j, whose completion frees the
-//           stage. Q' and P' sit in shared memory. Thread = key (S') or head dim
-//           (O'); row maxima cross the four warps through shared memory.
+//           full tiles' CTAs carry them instead of a CTA of their own: CTA mt of
+//           the MT Q tiles takes the key tiles j = mt (mod MT), so that the CTAs
+//           sharing each K/V tile through L2 keep the same pace, with transposed
+//           narrow products on those K/V tiles: S'^T = K Q'^T (M = 128 keys,
+//           N = 16 rows) right behind S_j, and O'^T += V^T P'^T (M = 128 head
+//           dims) right behind PV_j, whose completion then frees the stage. Q'
+//           and P' sit in shared memory. Thread = key (S') or head dim (O'); row
+//           maxima cross the four warps through shared memory. Each CTA writes
+//           its partial (O', m, l); tree_attn_xmerge_kernel merges them.
 // Every mbarrier wait is bounded (a few seconds of clock cycles); on expiry the
 // thread records a code in a device error word and leaves its loop.
 #include <cuda.h>
