@@ -246,6 +246,20 @@ def test_attention_gqa_groups(Hq, Hkv, branching):
         check_attention(w, si, st.O, [(b, kv) for b in range(w.B) for kv in (0, Hkv // 2, Hkv - 1)])
 
 
+@pytest.mark.parametrize("G,branching", [(3, (6, 6)), (5, (5, 4)), (7, (6, 5)), (6, (7, 2)), (7, (6, 2)),
+                                        (6, (8, 7)), (3, (4, 2, 2, 1)), (8, (4, 3))])
+def test_attention_every_leftover_size(G, branching):
+    """Query rows per KV head = 128 * MT + R for R = 1..8 (the rows past the full tiles ride with
+    the MT full-tile CTAs on interleaved key tiles): single and split KV ranges, an empty prefix."""
+    dev = gpu_ready()
+    for B, L_range in ((1, (700, 700)), (5, (0, 400))):
+        w = configs.scaled(configs.get("gqa7b_b32"), B=B, d=64, V=64, Hq=2 * G, Hkv=2, branching=branching,
+                           L_range=L_range)
+        si = synth.make_step_inputs(w, seed=G * 10 + len(branching) + B, device=dev)
+        st = run_attention(w, si, dev)
+        check_attention(w, si, st.O, [(b, kv) for b in range(w.B) for kv in range(w.Hkv)])
+
+
 @pytest.mark.parametrize("name", NAMES[1:])
 def test_attention_full_size_sampled(name):
     dev = gpu_ready()
