@@ -37,10 +37,8 @@ UNIT = "steps/s"
 DEFAULT_WORKLOAD = "vicuna7b_b1"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes per medusa_heads call, from the committed ncu capture of the heads
-# kernels on a reduced vocabulary (V=8000: traffic 1.02x the algorithmic
-# weight bytes), scaled to the workload's weight rows. Absent = not captured.
-# dram read + write of the dominant call's kernels, one call (ncu captures summarised in profiles/)
+# DRAM bytes (read + write) of one call of the step's dominant call, from full-size ncu captures
+# of its kernels (one pass each; summarised in profiles/). Absent = not captured: traffic null.
 NCU_TRAFFIC_BYTES = {"vicuna7b_b1": 1189250048, "vicuna7b_b1_shared": 402850048, "vicuna13b_b8": 1918169600}   # medusa_heads
 NCU_ATTN_TRAFFIC_BYTES = {"gqa7b_b32": 1512225024, "vicuna33b_b16": 3573720576}   # medusa_tree_attention
 
