@@ -831,7 +831,7 @@ bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Q-tile CTAs per (sequence, KV head): a short remainder rides with the last full tile.
+// Q-tile CTAs per (sequence, KV head): a short remainder of rows rides with the full tiles' CTAs.
 cudaError_t attention_tc_take_error(uint32_t* out, cudaStream_t st) {
   static const uint32_t zero = 0;
   cudaError_t e =
