@@ -32,6 +32,21 @@ def test_header_declares_the_five_steps():
         assert n in names
 
 
+@pytest.mark.parametrize("lang,std", [("c", "-std=c11"), ("c++", "-std=c++17")])
+def test_header_is_plain_c_and_cpp(lang, std):
+    """include/medusa.h compiles on its own as C11 (pedantic) and as C++17: a C caller needs nothing else."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = '#include "medusa.h"\nint main(void) { medusa_cfg c; medusa_step_args a; (void)c; (void)a; return 0; }\n'
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    r = subprocess.run([cc, "-x", lang, std, "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only", "-I", inc, "-"],
+                       input=src, text=True, capture_output=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in declared_entry_points():
         assert hasattr(lib, name), name
