@@ -186,12 +186,15 @@ def test_inverse_cdf_brute_force():
         assert y == ref and w[y] > 0
 
 
-def _tree_walk_first_token(p, q, s, n, seed):
-    """First emitted token of the tree walk, depth-1 tree whose s drafts are sampled from q."""
+def _tree_walk_first_token(p, q, s, n, seed, T=1.0):
+    """First emitted token of the tree walk, depth-1 tree whose s drafts are sampled from q.
+
+    The logits handed to the walk are T * log(p) and T * log(q), so a walk that
+    divides by T before its softmax sees exactly p and q."""
     V = p.shape[0]
     branching = (s,)
-    t_log = np.log(p)[None].repeat(1 + s, axis=0)
-    h_log = np.log(q)[None]
+    t_log = T * np.log(p)[None].repeat(1 + s, axis=0)
+    h_log = T * np.log(q)[None]
     counts = np.zeros(V)
     ks = np.arange(n)
     ud = philox_uniforms(seed, ks[:, None], np.arange(s)[None, :], 10)
@@ -202,7 +205,7 @@ def _tree_walk_first_token(p, q, s, n, seed):
         drafts = [O.inverse_cdf(q, float(ud[i, j]))[0] for j in range(s)]
         tokens = np.array([0] + drafts)
         acc, path, out, n_out, _ = O.verify_rejection(
-            tokens, lay["parent"], t_log, h_log, ua[i][None, :], np.array([ur[i], 0.5]), 1, 1.0)
+            tokens, lay["parent"], t_log, h_log, ua[i][None, :], np.array([ur[i], 0.5]), 1, T)
         counts[out[0]] += 1
     return counts / n
 
@@ -287,3 +290,110 @@ def test_pins_catch_a_walk_that_forgets_the_residual(monkeypatch):
     p, q = _pq(21)
     emp = _tree_walk_first_token(p, q, 2, 40000, seed=3)
     assert 0.5 * np.abs(emp - p).sum() > GOLD["rs_monte_carlo"]["tvd_tolerance"]
+
+
+# --------------------------------------------------------------------------- temperature
+# "Medusa 심층 아키텍처", section "수학적 무손실 보장": p and q are the target's and the
+# draft's distributions at the sampling temperature, softmax(logits / T). The pins
+# below fix the division by T without restating it: logits built as T * log(w)
+# must give back w / sum(w) exactly, T -> 0 must give the argmax and T -> inf the
+# uniform law, and the walk fed T * log(p) must emit p.
+TEMPS = (0.5, 0.7, 1.3, 2.0)
+
+
+def _softmax_t_weight_error(T):
+    """max |softmax_t(T log w + c, T) - w / sum w| over a few positive weight vectors."""
+    worst = 0.0
+    for w in ([1.0, 2.0, 3.0, 4.0], [0.05, 0.7, 0.25], [3.0, 1.0, 1.0, 1.0, 2.0, 0.5, 0.25, 0.25]):
+        w = np.array(w)
+        for c in (0.0, -17.5, 40.0):              # a constant shift of every logit changes nothing
+            got = O.softmax_t(T * np.log(w) + c, T)
+            worst = max(worst, float(np.abs(got - w / w.sum()).max()))
+    return worst
+
+
+@pytest.mark.parametrize("T", TEMPS)
+def test_softmax_t_recovers_weights(T):
+    assert _softmax_t_weight_error(T) < 1e-14
+
+
+def test_softmax_t_hand_values():
+    """Two-token cases worked by hand: logits (0, ln 2) at T = 1/2 are (0, ln 4) -> (1/5, 4/5);
+    at T = 2 they are (0, ln sqrt 2) -> (1/(1+sqrt 2), sqrt 2/(1+sqrt 2)); logits (0, ln 3) at
+    T = 0.7 weigh 1 : 3^(1/0.7)."""
+    x = np.array([0.0, math.log(2.0)])
+    np.testing.assert_allclose(O.softmax_t(x, 0.5), [0.2, 0.8], rtol=0, atol=1e-15)
+    r2 = math.sqrt(2.0)
+    np.testing.assert_allclose(O.softmax_t(x, 2.0), [1 / (1 + r2), r2 / (1 + r2)], rtol=0, atol=1e-15)
+    w = 3.0 ** (1 / 0.7)                                   # 4.797... : ln 3 / 0.7 exponentiated
+    np.testing.assert_allclose(O.softmax_t(np.array([0.0, math.log(3.0)]), 0.7), [1 / (1 + w), w / (1 + w)],
+                               rtol=0, atol=1e-15)
+
+
+def test_softmax_t_limits():
+    """T -> 0 concentrates on the largest logit; T -> inf spreads evenly."""
+    x = np.array([0.3, 1.0, -2.0, 0.99, 1.0 - 1e-3])
+    cold = O.softmax_t(x, 1e-5)
+    assert abs(cold[1] - 1.0) < 1e-12 and cold.sum() == pytest.approx(1.0, abs=1e-15)
+    hot = O.softmax_t(x, 1e6)
+    np.testing.assert_allclose(hot, np.full(5, 0.2), rtol=0, atol=1e-6)
+    # a lower temperature sharpens: the largest probability grows as T falls
+    tops = [O.softmax_t(x, T).max() for T in (4.0, 2.0, 1.0, 0.7, 0.5)]
+    assert all(a < b for a, b in zip(tops, tops[1:]))
+
+
+@pytest.mark.parametrize("T", (0.7, 2.0))
+@pytest.mark.parametrize("seed", range(3))
+def test_exact_enumeration_tempered(T, seed):
+    """The single-draft rule at temperature T on vocab 8: p and q come from logits T log p0
+    and T log q0, the enumerated output law is p0 to 1e-12."""
+    p0, q0 = _pq(seed)
+    p = O.softmax_t(T * np.log(p0), T)
+    q = O.softmax_t(T * np.log(q0), T)
+    V = p0.shape[0]
+    res = O.residual(p, q)
+    final = np.zeros(V)
+    for x in range(V):
+        a = O.acceptance_ratio(p, q, x)
+        final[x] += q[x] * a
+        final += q[x] * (1 - a) * res
+    np.testing.assert_allclose(final, p0, rtol=0, atol=1e-12)
+
+
+def test_monte_carlo_tree_walk_tempered():
+    """The tree walk at T = 0.7 with drafts sampled from q emits p: target and head
+    logits are T log p and T log q, 150k samples, total variation below 0.01."""
+    ex = GOLD["rs_monte_carlo"]
+    p, q = _pq(21)
+    emp = _tree_walk_first_token(p, q, 2, ex["samples"], seed=41, T=0.7)
+    assert 0.5 * np.abs(emp - p).sum() < ex["tvd_tolerance"]
+
+
+def test_pins_catch_a_temperature_multiplied_instead_of_divided(monkeypatch):
+    """softmax(x * T) in place of softmax(x / T) fails the weight pin, the hand values and the
+    tempered walk."""
+    def wrong(x, T):
+        y = np.asarray(x, dtype=np.float64) * T
+        e = np.exp(y - y.max())
+        return e / e.sum()
+    monkeypatch.setattr(O, "softmax_t", wrong)
+    for T in TEMPS:
+        assert _softmax_t_weight_error(T) > 1e-2
+    with pytest.raises(AssertionError):
+        test_softmax_t_hand_values()
+    p, q = _pq(21)
+    emp = _tree_walk_first_token(p, q, 2, 20000, seed=43, T=0.7)
+    assert 0.5 * np.abs(emp - p).sum() > GOLD["rs_monte_carlo"]["tvd_tolerance"]
+
+
+def test_pins_catch_a_temperature_ignored(monkeypatch):
+    """A softmax that forgets T fails the weight pin at every T != 1."""
+    monkeypatch.setattr(O, "softmax_t", lambda x, T: _plain_softmax(x))
+    for T in TEMPS:
+        assert _softmax_t_weight_error(T) > 1e-2
+
+
+def _plain_softmax(x):
+    y = np.asarray(x, dtype=np.float64)
+    e = np.exp(y - y.max())
+    return e / e.sum()
