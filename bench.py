@@ -7,10 +7,13 @@ top-s) -> candidate tree -> tree attention -> acceptance -> KV compaction.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-N > 1 runs one independent replica per GPU (launched by torch.distributed.run);
-the step has no exchange, so there is no collective on the data path and the
-scaling is weak. `--impl reference` times the CPU oracle (plain float64
-numpy) on the host cores instead.
+N > 1 runs one independent replica per GPU under torch.distributed.run (this
+script starts the launcher itself when it is run plainly, and refuses a
+launcher whose WORLD_SIZE differs from N); the step has no exchange, so there
+is no collective on the data path and the scaling is weak. The default
+workload is the largest one that fits one GPU (vicuna33b_b16). `--impl
+reference` times the CPU oracle (plain float64 numpy, single-threaded BLAS) on
+the host cores instead.
 """
 from __future__ import annotations
 
@@ -26,6 +29,12 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# The CPU oracle is timed single-threaded: its numpy matmuls would otherwise use every host
+# core through the BLAS thread pool. Set before numpy loads its BLAS; a value already in the
+# environment wins, and the line reports the thread count the pool actually has.
+for _var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_var, "1")
+
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
@@ -34,7 +43,8 @@ from medusa_speculative_decoding_heads_gb300.configs import F32, GREEDY, REJECTI
 
 METRIC = "Medusa verify steps/s (heads+tree-attn+accept); HBM GB/s vs 8 TB/s"
 UNIT = "steps/s"
-DEFAULT_WORKLOAD = "vicuna7b_b1"
+# the largest workload that fits one GPU: 33B-shaped heads over a batch of 16, 5.6 GB per step
+DEFAULT_WORKLOAD = "vicuna33b_b16"
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) of one call of the step's dominant call, from full-size ncu captures
@@ -161,40 +171,81 @@ def dist_env():
 
 
 # ----------------------------------------------------------------------------- CPU oracle timing
-def oracle_inputs_from(si, tl):
+# At most this many sequences of a batch go through the oracle's per-sequence parts (tree,
+# attention, acceptance, compaction) in one timed oracle step; the float64 copy of a 33B-shaped
+# sequence's KV cache alone is 0.9 GB, and its attention takes about a second on one core. The
+# heads always run over the whole batch.
+ORACLE_SEQS = 1
+
+
+def oracle_inputs_from(si, tl, seqs):
+    """Host float64 inputs of the oracle: the heads' inputs for the whole batch, the
+    per-sequence inputs (Q, cache, target logits, uniforms, lengths) of the first `seqs`."""
     f = lambda t: t.detach().to("cpu", torch.float32).double().numpy()
+    n = seqs
     return {"h": f(si.h), "W": f(si.W), "b": None if si.bias is None else f(si.bias), "U": f(si.U),
-            "Q": f(si.Q), "Kc": f(si.Kc), "Vc": f(si.Vc), "tl": f(tl), "root": si.root_token, "L": si.L,
-            "L_cap": si.L_cap, "u_acc": si.u_acc, "u_res": si.u_res}
+            "Q": f(si.Q[:n]), "Kc": f(si.Kc[:n]), "Vc": f(si.Vc[:n]), "tl": f(tl[:n]), "root": si.root_token[:n],
+            "L": si.L[:n], "L_cap": si.L_cap, "u_acc": si.u_acc[:n], "u_res": si.u_res[:n], "seqs": n,
+            "B": int(si.h.shape[0])}
 
 
 def oracle_step(O, w, mode, x):
+    """One oracle step: heads over the whole batch, then the per-sequence parts over the
+    sampled sequences. Returns (seconds in the heads, seconds in the rest)."""
+    t0 = time.perf_counter()
     r, z = O.medusa_heads(x["h"], x["W"], x["b"], x["U"])
+    t1 = time.perf_counter()
+    z = z[:x["seqs"]]
     topk, _ = O.heads_top_s(z, w.branching)
     tree = O.tree_build(w.branching, x["root"], topk, x["L"], x["L_cap"], paths=w.tree_paths)
     O.tree_attention(x["Q"], x["Kc"], x["Vc"], x["L"], tree["mask"], w.Hq, w.Hkv)
     ver = O.verify_batch(mode, tree, x["tl"], w.K, head_logits=z, u_acc=x["u_acc"], u_res=x["u_res"],
                          T=w.temperature)
-    O.kv_compact(x["Kc"], x["Vc"], x["L"], ver["acc"], ver["path"])
-    return ver
+    # compaction moves rows inside each sequence's tree region only; the oracle gets that region
+    # (committed length 0 there) instead of copying the whole float64 cache
+    N = tree["N"]
+    kr = np.stack([x["Kc"][b, :, int(x["L"][b]):int(x["L"][b]) + N] for b in range(x["seqs"])])
+    vr = np.stack([x["Vc"][b, :, int(x["L"][b]):int(x["L"][b]) + N] for b in range(x["seqs"])])
+    O.kv_compact(kr, vr, np.zeros(x["seqs"], dtype=np.int64), ver["acc"], ver["path"])
+    return t1 - t0, time.perf_counter() - t1
 
 
 def time_oracle(w, mode, x, steps, warmup=0, budget_s=None):
+    """Seconds per whole-batch oracle step: the heads' time plus the sampled sequences'
+    time scaled to the batch (B / seqs)."""
     from oracle import medusa_oracle as O
     for _ in range(warmup):
         oracle_step(O, w, mode, x)
+    scale = x["B"] / x["seqs"]
     times = []
     t_all = time.perf_counter()
     for _ in range(steps):
-        t0 = time.perf_counter()
-        oracle_step(O, w, mode, x)
-        times.append(time.perf_counter() - t0)
+        th, tr = oracle_step(O, w, mode, x)
+        times.append(th + scale * tr)
         if budget_s is not None and time.perf_counter() - t_all > budget_s:
             break
     return times
 
 
-def cpu_cores():
+def oracle_sample_text(w, x, n):
+    if x["seqs"] == x["B"]:
+        return (f"{n} full oracle steps of {w.name} (B={w.B}; compaction of the tree region), float64 numpy, "
+                f"single-threaded BLAS, inputs pre-decoded")
+    seqs = "sequence 0" if x["seqs"] == 1 else f"sequences 0..{x['seqs'] - 1}"
+    return (f"{n} oracle steps of {w.name}: heads over all {x['B']} sequences, then tree, attention, acceptance "
+            f"and compaction (of the tree region) for {seqs}, that part's time scaled by {x['B']}/{x['seqs']}; "
+            f"float64 numpy, single-threaded BLAS, inputs pre-decoded")
+
+
+def blas_threads():
+    """Threads of the BLAS pool numpy uses (threadpoolctl when present, else the environment)."""
+    try:
+        import threadpoolctl
+        n = [i["num_threads"] for i in threadpoolctl.threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except ImportError:
+        pass
     for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
         if os.environ.get(var):
             return int(os.environ[var])
@@ -225,7 +276,7 @@ def run_reference(args):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     si = synth.make_step_inputs(w, seed=args.seed, device=dev)
     tl = make_targets(w, si, dev, mode, args.seed, via_library=False)
-    x = oracle_inputs_from(si, tl)
+    x = oracle_inputs_from(si, tl, min(w.B, ORACLE_SEQS))
     L = np.asarray(si.L)
     del si, tl
     if dev == "cuda":
@@ -237,8 +288,8 @@ def run_reference(args):
             "steps": len(times), "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(w, L, mode, args.gpus),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                             "sample": f"one full oracle step of {w.name} (B={w.B}) per timed step"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                             "sample": oracle_sample_text(w, x, len(times))},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -631,14 +682,34 @@ def run_e2e(w, st, inp, L0, tl, si, args, stream, world):
 
 
 def cpu_baseline(w, mode, si, tl):
-    x = oracle_inputs_from(si, tl)
+    x = oracle_inputs_from(si, tl, min(w.B, ORACLE_SEQS))
     times = time_oracle(w, mode, x, steps=50, warmup=1, budget_s=15.0)
-    return {"value": len(times) / sum(times), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{len(times)} full oracle steps of {w.name} (B={w.B}), float64 numpy, inputs pre-decoded"}
+    return {"value": len(times) / sum(times), "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": oracle_sample_text(w, x, len(times))}
+
+
+def launch_replicas(args):
+    """`--gpus N` without a launcher: start N ranks of this script under torch.distributed.run
+    (one per GPU, rendezvous on 127.0.0.1). Returns the launcher's exit status."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
 
 
 def main():
     args = parse()
+    _, world, _ = dist_env()
+    if args.gpus < 1:
+        sys.exit("--gpus must be at least 1")
+    if "WORLD_SIZE" in os.environ and world != args.gpus:
+        sys.exit(f"--gpus {args.gpus} but the launcher started {world} ranks")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        if args.impl == "ours" and args.part == "step":
+            return launch_replicas(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.part != "step":

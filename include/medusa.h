@@ -278,8 +278,15 @@ MEDUSA_API int medusa_kv_commit_paged(const medusa_cfg* cfg, void* Kp, void* Vp,
  * MEDUSA_NOALLOC_SCRATCH_BYTES that the library holds on every GPU that loads
  * it, until the process exits.
  *   - Returns MEDUSA_ERR_UNSUPPORTED, enqueueing nothing, when the
- *     configuration needs more scratch than that (medusa_workspace_size
- *     minus the heads part; B * N * Hq * (D + 2) * 4 bytes per KV split).
+ *     configuration needs more scratch than that. The scratch it needs is the
+ *     tree-attention share of medusa_workspace_size: B * S * N * Hq * D * 4
+ *     bytes of partial outputs and B * S * N * Hq * 2 * 4 bytes of running
+ *     maxima and sums for the S KV splits the library picks (1 <= S <= 32,
+ *     more only while the grid fits one wave), plus, on the bf16 D = 128
+ *     path when a KV head's N * Hq / Hkv query rows leave 1..8 rows past its
+ *     full 128-row tiles, B * Hkv * S * (full tiles) * 8 * (D + 2) * 4 bytes
+ *     for those rows; each part is rounded up to 256 bytes. A refusal is
+ *     immediate, so one call at set-up tells a caller whether a shape fits.
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any

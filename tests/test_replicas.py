@@ -62,3 +62,29 @@ def test_single_rank_is_local():
     ms, value = bench.replica_throughput(20.0, steps=10, world=1, device="cpu")
     assert ms == 20.0 and value == pytest.approx(500.0)
     assert bench.replica_seed(3, 0) == 3 and bench.replica_seed(3, 1) != 3
+
+
+def test_gpus_flag_must_match_the_launcher():
+    """`--gpus 2` under a launcher that started a different number of ranks is refused
+    before any GPU work."""
+    import subprocess
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "1"],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0 and "--gpus 2" in r.stderr
+
+
+def test_gpus_flag_starts_the_replicas(monkeypatch):
+    """`--gpus 4` run plainly re-launches the script as 4 ranks under torch.distributed.run."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    seen = {}
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--gpus", "4", "--steps", "3"])
+    monkeypatch.setattr(bench.subprocess, "call", lambda cmd: seen.setdefault("cmd", cmd) and 0)
+    assert bench.main() == 0
+    cmd = seen["cmd"]
+    assert cmd[1:3] == ["-m", "torch.distributed.run"] and "--nproc-per-node=4" in cmd
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert cmd[-4:] == ["--gpus", "4", "--steps", "3"]
