@@ -178,8 +178,8 @@ MEDUSA_API int medusa_tree_attention(const medusa_cfg* cfg, const void* Q, const
  *   (-1 pad); n_out [B] = acc + 1; flags [B] uint32: this call ORs in its
  *   MEDUSA_FLAG_* bits (clear or initialise it first, e.g. with medusa_tree_build);
  *   MEDUSA_FLAG_TIMEOUT marks a sequence whose walk gave up on a bounded wait.
- * GREEDY reduces every tree node's target row to its argmax in parallel first
- * (rows split over several CTAs), so the walk itself is a few table lookups.
+ * GREEDY walks each sequence on one CTA that reads only the target rows of
+ * the nodes it visits (acc + 1 rows), taking each row's argmax as it goes.
  * REJECTION reduces every head row (max and softmax normaliser) in parallel
  * first; each sequence's walk then runs on a cluster of up to 8 CTAs that split
  * the vocabulary and trade their partial sums through distributed shared

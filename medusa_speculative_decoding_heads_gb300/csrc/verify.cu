@@ -13,9 +13,10 @@
 // walk, siblings tried in rank order, the residual carried across siblings;
 // draws use inverse CDF (smallest y with cdf(y) > u * total).
 //
-// Two launches per call. Greedy: every tree node's target-row argmax in
-// parallel (one CTA per row), then a one-thread-per-sequence walk. Rejection
-// sampling: the max and softmax normaliser of every head's logit row in
+// Greedy: one launch, one CTA per sequence, which argmaxes the target row of
+// the current node, moves to the child carrying that token and repeats, so
+// only the acc + 1 rows the walk visits are read. Rejection sampling (two
+// launches): the max and softmax normaliser of every head's logit row in
 // parallel, then one cluster of CTAs per sequence walks, each CTA owning a slice
 // of the vocabulary; at each visited node one sweep gives the target row's max
 // and normaliser, an acceptance test is O(1), and only a rejection (the
@@ -186,7 +187,6 @@ __device__ __forceinline__ void load8<float>(const float* row, int v, float* x) 
 // ---------------------------------------------------------------- row pass (parallel)
 constexpr int kRowThreads = 256;
 constexpr int kRowWarps = kRowThreads / 32;
-constexpr int kMaxRowSlices = 8;   // CTAs per row in the greedy argmax pass
 constexpr int kMaxHsSlices = 8;    // CTAs per head row in the rejection-sampling stats pass
 
 // CTAs per row for a pass over `rows` rows of V entries: enough for about two
@@ -198,86 +198,6 @@ int row_slices(long rows, int V, int cap) {
   return (int)(p < by_len ? p : (by_len < 1 ? 1 : by_len));
 }
 int slice_len(int V, int P) { return ((V + P - 1) / P + 7) / 8 * 8; }
-
-// Greedy: the argmax of slice p of target row (b, n) (lowest index on ties),
-// part[(b * N + n) * P + p] = (value bits, index); grid (P, N, B). The walk
-// merges the P slices of the rows it visits with the same rule, which gives
-// the argmax of the whole row. VEC: slices start at multiples of 8 and are read
-// 8 entries at a time (V % 8 == 0), all of a thread's loads in flight.
-template <typename T, bool VEC>
-__global__ void __launch_bounds__(kRowThreads)
-row_argmax_kernel(const T* __restrict__ tl, int N, int V, int chunk, int2* __restrict__ part) {
-  pdl_wait();
-  pdl_trigger();
-  const int p = blockIdx.x, n = blockIdx.y, b = blockIdx.z, P = gridDim.x;
-  const T* row = tl + ((size_t)b * N + n) * V;
-  const int v0 = min(V, p * chunk), v1 = min(V, v0 + chunk);
-  float bv = -INFINITY;
-  int bi = 0x7fffffff;
-  if (VEC) {
-    constexpr int kU = 8;   // vectors per thread per round
-    for (int base = v0; base < v1; base += kU * 8 * kRowThreads) {
-      float x[kU][8];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int v = base + 8 * (threadIdx.x + u * kRowThreads);
-        if (v < v1) load8<T>(row, v, x[u]);
-        else
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[u][e] = -INFINITY;
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int v = base + 8 * (threadIdx.x + u * kRowThreads) + e;
-          if (v < v1 && better(x[u][e], v, bv, bi)) {
-            bv = x[u][e];
-            bi = v;
-          }
-        }
-    }
-  } else {
-#pragma unroll 4
-    for (int v = v0 + threadIdx.x; v < v1; v += kRowThreads) {
-      const float x = Elt<T>::load(row, v);
-      if (better(x, v, bv, bi)) {
-        bv = x;
-        bi = v;
-      }
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (better(ov, oi, bv, bi)) {
-      bv = ov;
-      bi = oi;
-    }
-  }
-  __shared__ float sv[kRowWarps];
-  __shared__ int si[kRowWarps];
-  if ((threadIdx.x & 31) == 0) {
-    sv[threadIdx.x >> 5] = bv;
-    si[threadIdx.x >> 5] = bi;
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    bv = threadIdx.x < kRowWarps ? sv[threadIdx.x] : -INFINITY;
-    bi = threadIdx.x < kRowWarps ? si[threadIdx.x] : 0x7fffffff;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (better(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (threadIdx.x == 0) part[((size_t)b * N + n) * P + p] = make_int2(__float_as_int(bv), bi);
-  }
-}
 
 // exp(y * c) for the bulk sums, c = log2(e) / T folded in by the caller: one
 // multiply and the hardware base-2 exponential. Relative error stays near
@@ -304,53 +224,123 @@ struct WalkOut {
   uint32_t* flags;
 };
 
-// The argmax of a whole target row from its P slice results.
-__device__ __forceinline__ int row_best(const int2* __restrict__ pr, int P) {
-  float bv = -INFINITY;
-  int bi = 0x7fffffff;
-  for (int p = 0; p < P; ++p) {
-    const int2 q = pr[p];
-    if (better(__int_as_float(q.x), q.y, bv, bi)) {
-      bv = __int_as_float(q.x);
-      bi = q.y;
-    }
-  }
-  return bi;
-}
+// Greedy walk, one CTA per sequence. At each visited node all threads take the
+// argmax of its target row (largest value, lowest token id among equal values:
+// 16-byte loads, eight in flight per thread, then warp and block reductions);
+// thread 0 looks for the child carrying that token among the node's children
+// (held in shared memory with the sequence's tokens) and the CTA descends or
+// stops. Rows the walk does not reach are never read.
+constexpr int kGwThreads = 512;
+constexpr int kGwWarps = kGwThreads / 32;
 
-// Greedy walk from the per-row argmax. One thread per sequence.
-__global__ void greedy_walk_kernel(TreeShape ts, int B, const int32_t* __restrict__ tokens,
-                                   const int32_t* __restrict__ parent, const int32_t* __restrict__ first_child,
-                                   const int2* __restrict__ part, int P, WalkOut w) {
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kGwThreads)
+greedy_walk_kernel(TreeShape ts, int V, const int32_t* __restrict__ tokens, const int32_t* __restrict__ parent,
+                   const int32_t* __restrict__ first_child, const T* __restrict__ tl, WalkOut w) {
+  __shared__ int s_tok[kMaxN], s_par[kMaxN], s_fc[kMaxN];
+  __shared__ float sv[kGwWarps];
+  __shared__ int si[kGwWarps];
+  __shared__ int s_next;
   pdl_wait();
   pdl_trigger();
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= B) return;
-  const int N = ts.N, K = ts.K;
-  const int32_t* tok = tokens + (size_t)b * N;
+  const int b = blockIdx.x, N = ts.N, K = ts.K;
+  for (int i = threadIdx.x; i < N; i += kGwThreads) {
+    s_tok[i] = tokens[(size_t)b * N + i];
+    s_par[i] = parent[i];
+    s_fc[i] = first_child[i];
+  }
   int32_t* path = w.path + (size_t)b * (K + 1);
   int32_t* out = w.out_tokens + (size_t)b * (K + 1);
   int cur = 0, acc = 0;
-  path[0] = 0;
-  for (int dep = 1; dep <= K; ++dep) {
-    const int a = row_best(part + ((size_t)b * N + cur) * P, P);
-    const int fc = first_child[cur];
-    int nx = -1;
-    for (int j = 0; fc >= 0 && fc + j < N && parent[fc + j] == cur; ++j)   // cur's children
-      if (tok[fc + j] == a) nx = fc + j;
+  if (threadIdx.x == 0) path[0] = 0;
+  while (true) {
+    const T* row = tl + ((size_t)b * N + cur) * V;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    if (VEC) {
+      constexpr int kU = 8;   // 16-byte vectors per thread per round
+      for (int base = 0; base < V; base += kU * 8 * kGwThreads) {
+        float x[kU][8];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int v = base + 8 * (threadIdx.x + u * kGwThreads);
+          if (v < V) load8<T>(row, v, x[u]);
+          else
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[u][e] = -INFINITY;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int v = base + 8 * (threadIdx.x + u * kGwThreads) + e;
+            if (v < V && better(x[u][e], v, bv, bi)) {
+              bv = x[u][e];
+              bi = v;
+            }
+          }
+      }
+    } else {
+#pragma unroll 4
+      for (int v = threadIdx.x; v < V; v += kGwThreads) {
+        const float x = Elt<T>::load(row, v);
+        if (better(x, v, bv, bi)) {
+          bv = x;
+          bi = v;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((threadIdx.x & 31) == 0) {
+      sv[threadIdx.x >> 5] = bv;
+      si[threadIdx.x >> 5] = bi;
+    }
+    __syncthreads();   // also publishes the tree arrays on the first pass
+    if (threadIdx.x < 32) {
+      bv = threadIdx.x < kGwWarps ? sv[threadIdx.x] : -INFINITY;
+      bi = threadIdx.x < kGwWarps ? si[threadIdx.x] : 0x7fffffff;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (threadIdx.x == 0) {
+        // bi is the target's token after `cur`: the next draft if a child carries it, else the bonus
+        int nx = -1;
+        const int fc = acc < K ? s_fc[cur] : -1;
+        for (int j = 0; fc >= 0 && fc + j < N && s_par[fc + j] == cur; ++j)
+          if (s_tok[fc + j] == bi) nx = fc + j;
+        out[acc] = bi;
+        if (nx >= 0) path[acc + 1] = nx;
+        s_next = nx;
+      }
+    }
+    __syncthreads();
+    const int nx = s_next;
     if (nx < 0) break;
-    out[acc] = a;
     cur = nx;
     ++acc;
-    path[acc] = cur;
   }
-  out[acc] = row_best(part + ((size_t)b * N + cur) * P, P);
-  for (int r = acc + 1; r <= K; ++r) {
-    path[r] = -1;
-    out[r] = -1;
+  if (threadIdx.x == 0) {
+    for (int r = acc + 1; r <= K; ++r) {
+      path[r] = -1;
+      out[r] = -1;
+    }
+    w.acc[b] = acc;
+    w.n_out[b] = acc + 1;
   }
-  w.acc[b] = acc;
-  w.n_out[b] = acc + 1;
 }
 
 constexpr int kVThreads = 256;
@@ -995,20 +985,12 @@ cudaError_t run_rs(const medusa_cfg& c, const TreeShape& ts, const int32_t* toke
 
 template <typename T>
 cudaError_t run_greedy(const medusa_cfg& c, const TreeShape& ts, const int32_t* tokens, const int32_t* parent,
-                       const int32_t* first_child,
-                       const void* tl, const WalkOut& w, int2* part, cudaStream_t st) {
-  const int P = row_slices((long)c.B * ts.N, c.V, kMaxRowSlices);
-  const int chunk = slice_len(c.V, P);
+                       const int32_t* first_child, const void* tl, const WalkOut& w, cudaStream_t st) {
+  const T* rows = static_cast<const T*>(tl);
   if (c.V % 8 == 0)
-    launch_pdl(row_argmax_kernel<T, true>, dim3(P, ts.N, c.B), kRowThreads, 0, st, static_cast<const T*>(tl), ts.N, c.V,
-               chunk, part);
+    launch_pdl(greedy_walk_kernel<T, true>, c.B, kGwThreads, 0, st, ts, c.V, tokens, parent, first_child, rows, w);
   else
-    launch_pdl(row_argmax_kernel<T, false>, dim3(P, ts.N, c.B), kRowThreads, 0, st, static_cast<const T*>(tl), ts.N, c.V,
-               chunk, part);
-  note_launches(1);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  launch_pdl(greedy_walk_kernel, (c.B + 127) / 128, 128, 0, st, ts, c.B, tokens, parent, first_child, part, P, w);
+    launch_pdl(greedy_walk_kernel<T, false>, c.B, kGwThreads, 0, st, ts, c.V, tokens, parent, first_child, rows, w);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -1017,9 +999,7 @@ cudaError_t run_greedy(const medusa_cfg& c, const TreeShape& ts, const int32_t* 
 
 size_t verify_workspace(const medusa_cfg& c) {
   const TreeShape ts = tree_shape(c);
-  const size_t greedy = (size_t)c.B * ts.N * kMaxRowSlices * sizeof(int2);
-  const size_t rs = (size_t)c.B * ts.K * kMaxHsSlices * sizeof(float2);
-  return align_up(greedy > rs ? greedy : rs, 256);
+  return align_up((size_t)c.B * ts.K * kMaxHsSlices * sizeof(float2), 256);   // head-row statistics (rejection)
 }
 
 cudaError_t launch_verify(const medusa_cfg& c, const int32_t* tokens, const int32_t* parent, const int32_t* first_child,
@@ -1028,11 +1008,9 @@ cudaError_t launch_verify(const medusa_cfg& c, const int32_t* tokens, const int3
                           cudaStream_t st) {
   const TreeShape ts = tree_shape(c);
   WalkOut w{acc, path, out_tokens, n_out, flags};
-  if (c.mode == MEDUSA_GREEDY) {
-    int2* part = static_cast<int2*>(ws);
-    return c.dtype == MEDUSA_F32 ? run_greedy<float>(c, ts, tokens, parent, first_child, tl, w, part, st)
-                                 : run_greedy<uint16_t>(c, ts, tokens, parent, first_child, tl, w, part, st);
-  }
+  if (c.mode == MEDUSA_GREEDY)
+    return c.dtype == MEDUSA_F32 ? run_greedy<float>(c, ts, tokens, parent, first_child, tl, w, st)
+                                 : run_greedy<uint16_t>(c, ts, tokens, parent, first_child, tl, w, st);
   float2* stats = static_cast<float2*>(ws);
   return c.dtype == MEDUSA_F32 ? run_rs<float>(c, ts, tokens, parent, first_child, tl, hl, u_acc, u_res, w, stats, st)
                                : run_rs<uint16_t>(c, ts, tokens, parent, first_child, tl, hl, u_acc, u_res, w, stats, st);

@@ -315,6 +315,22 @@ def test_verify_greedy_bit_exact(name):
     assert len(set(ref["acc"].tolist())) > 1
 
 
+@pytest.mark.parametrize("V", [3001, 13, 16])
+def test_verify_greedy_ragged_vocab(V):
+    """Vocabularies that are not a multiple of 8 (one entry at a time) and the smallest ones;
+    planted paths of every depth, B = 24."""
+    dev = gpu_ready()
+    w = configs.scaled(configs.get("vicuna13b_b8"), B=24, V=V, target_corr=0.0, modes=(GREEDY,))
+    L, L_cap, root, topk, tree, tl, depths = greedy_case(w, dev, seed=V)
+    st = DeviceStep(w, GREEDY, L_cap, dev)
+    st.tree_build(torch.from_numpy(root).to(dev), torch.from_numpy(L).to(dev), topk=torch.from_numpy(topk).to(dev))
+    st.verify(tl)
+    torch.cuda.synchronize()
+    ref = O.verify_batch(GREEDY, tree, f64(tl), w.K)
+    for key in ("acc", "path", "out_tokens", "n_out"):
+        assert np.array_equal(i64(getattr(st, key)), ref[key]), key
+
+
 @pytest.mark.parametrize("name", ["vicuna7b_b1", "vicuna33b_b16"])
 def test_repeated_calls_share_workspace(name):
     """A workspace carries nothing from one call into the next: the same heads
