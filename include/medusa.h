@@ -67,7 +67,8 @@ enum {
   MEDUSA_ERR_UNSUPPORTED = -2, /* valid but outside the built limits          */
   MEDUSA_ERR_CAPACITY = -3,    /* host-visible capacity violation              */
   MEDUSA_ERR_CUDA = -4,        /* a CUDA launch or attribute call failed       */
-  MEDUSA_ERR_TIMEOUT = -5      /* a bounded device-side wait expired (medusa_poll_errors) */
+  MEDUSA_ERR_TIMEOUT = -5,     /* a bounded device-side wait expired (medusa_poll_errors) */
+  MEDUSA_ERR_BOUNDS = -6       /* checked build: a kernel met an out-of-range index (medusa_poll_checks) */
 };
 
 /* Per-sequence flag bits (uint32). */
@@ -261,7 +262,9 @@ MEDUSA_API int medusa_tree_attention_paged(const medusa_cfg* cfg, const void* Q,
  * path[b][r] in every KV head; then L_b += acc_b + 1 (in/out) and kv_map as for
  * medusa_kv_compact. Sequences with L_b < 0 or L_b + N > L_cap are left as they
  * are (kv_map = -1). Layouts and page_rows as for medusa_tree_attention_paged
- * (any dtype and D). */
+ * (any dtype and D). A row whose block-table page id lies outside
+ * [0, pool_layer_elems / (Hkv * page_rows * D)) is not written (when
+ * pool_layer_elems is 0, with one layer, page ids are not range-checked). */
 MEDUSA_API int medusa_kv_commit_paged(const medusa_cfg* cfg, void* Kp, void* Vp, int32_t page_rows,
                            const int32_t* block_table, const void* Kt, const void* Vt, int32_t n_layers,
                            size_t pool_layer_elems, size_t tree_layer_elems, int32_t* L, const int32_t* acc,
@@ -321,6 +324,29 @@ MEDUSA_API int medusa_poll_errors(medusa_stream_t stream, uint32_t* heads_codes,
  * MEDUSA_ERR_TIMEOUT with that bit set in *attention_codes. */
 #define MEDUSA_WAIT_SELFTEST_CODE 0x80000000u
 MEDUSA_API int medusa_selftest_wait_timeout(uint32_t budget_us, medusa_stream_t stream);
+
+/* Checked build. The library built with -DMEDUSA_CHECKED (libmedusa_checked.so)
+ * runs the same kernels with range checks on every index they read from device
+ * memory: root and top-s token ids (medusa_tree_build: [0, V)), the tree links
+ * and child tokens a walk follows (medusa_verify), acc and the path's node ids
+ * (medusa_kv_compact and medusa_kv_commit_paged: acc in [0, K], node ids in
+ * [0, N), each deeper than the one before), and block-table page ids
+ * (the paged calls: [0, pages)). Every build already clamps such an index or
+ * skips the access it would make; the checked build also ORs the matching
+ * MEDUSA_CHECK_* bit into a device word. Nothing traps.
+ * medusa_checked_build returns 1 in the checked build, 0 otherwise.
+ * medusa_poll_checks reads and clears those words in stream order, then
+ * synchronises `stream`: MEDUSA_OK when no check failed since the last poll (and
+ * always in the normal build, with *codes = 0), MEDUSA_ERR_BOUNDS when one did
+ * (*codes, a host pointer that may be NULL, receives the OR of the bits),
+ * MEDUSA_ERR_CUDA on a CUDA error. Not capturable in a CUDA graph. No
+ * counterpart on the pages: a debug aid. */
+#define MEDUSA_CHECK_TOKEN 0x1u  /* a token id outside [0, V)                                */
+#define MEDUSA_CHECK_TREE 0x2u   /* a parent / first-child link outside the tree or inconsistent */
+#define MEDUSA_CHECK_PATH 0x4u   /* acc outside [0, K] or a path node outside [0, N) / not deeper */
+#define MEDUSA_CHECK_PAGE 0x8u   /* a block-table page id outside the pool                   */
+MEDUSA_API int medusa_checked_build(void);
+MEDUSA_API int medusa_poll_checks(medusa_stream_t stream, uint32_t* codes);
 
 /* Number of kernels this library has enqueued in this process so far (host-side
  * counter, for diagnostics; no counterpart on the pages). */

@@ -14,6 +14,8 @@ from typing import Optional, Sequence, Tuple
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmedusa.so")
+# the same kernels built with device-side range checks (MEDUSA_CHECKED=1 in the environment selects it)
+LIB_CHECKED_PATH = os.path.join(PKG, "libmedusa_checked.so")
 
 F32, BF16 = 0, 1
 GREEDY, REJECTION = 0, 1
@@ -23,7 +25,9 @@ ENTRY_POINTS = ("medusa_node_count", "medusa_workspace_size", "medusa_heads", "m
                 "medusa_tree_attention", "medusa_verify", "medusa_kv_compact", "medusa_tree_attention_noalloc",
                 "medusa_tree_attention_paged", "medusa_kv_commit_paged", "medusa_step_graph_create",
                 "medusa_step_graph_launch", "medusa_step_graph_destroy", "medusa_poll_errors",
-                "medusa_selftest_wait_timeout", "medusa_launch_count", "medusa_status_string")
+                "medusa_selftest_wait_timeout", "medusa_checked_build", "medusa_poll_checks",
+                "medusa_launch_count", "medusa_status_string")
+CHECK_TOKEN, CHECK_TREE, CHECK_PATH, CHECK_PAGE = 1, 2, 4, 8
 
 
 class MedusaError(RuntimeError):
@@ -72,11 +76,17 @@ _lib: Optional[ctypes.CDLL] = None
 P = ctypes.c_void_p
 
 
-def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libmedusa.so (build it first with ``_build.build()``)."""
+def default_path() -> str:
+    return LIB_CHECKED_PATH if os.environ.get("MEDUSA_CHECKED") == "1" else LIB_PATH
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libmedusa.so, or libmedusa_checked.so when MEDUSA_CHECKED=1 is set (build them
+    first with ``_build.build()``)."""
     global _lib
     if _lib is not None:
         return _lib
+    path = path or default_path()
     if not os.path.exists(path):
         raise RuntimeError(f"libmedusa not built: {path} is missing (run __graft_entry__.build())")
     lib = ctypes.CDLL(path)
@@ -98,6 +108,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "medusa_step_graph_launch": [P, P],
         "medusa_step_graph_destroy": [P],
         "medusa_selftest_wait_timeout": [ctypes.c_uint32, P],
+        "medusa_checked_build": [],
+        "medusa_poll_checks": [P, ctypes.POINTER(ctypes.c_uint32)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -177,6 +189,26 @@ def poll_errors(stream=None):
     if s not in (0, STATUS_TIMEOUT):
         _check("medusa_poll_errors", s)
     return s, int(h.value), int(a.value)
+
+
+STATUS_BOUNDS = -6
+
+
+def checked_build() -> bool:
+    """True when the loaded library is the range-checked build."""
+    return bool(load().medusa_checked_build())
+
+
+def poll_checks(stream=None):
+    """Read and clear the checked build's range-check words (synchronises the stream).
+
+    Returns (status, codes); status is 0 or -6 (an out-of-range index was met), codes the
+    OR of the CHECK_* bits (always (0, 0) in the normal build)."""
+    c = ctypes.c_uint32()
+    s = load().medusa_poll_checks(_stream(stream), ctypes.byref(c))
+    if s not in (0, STATUS_BOUNDS):
+        _check("medusa_poll_checks", s)
+    return s, int(c.value)
 
 
 def selftest_wait_timeout(budget_us: int, stream=None) -> None:

@@ -199,7 +199,11 @@ int medusa_kv_commit_paged(const medusa_cfg* cfg, void* Kp, void* Vp, int32_t pa
   if (!aligned16(Kp) || !aligned16(Vp) || !aligned16(Kt) || !aligned16(Vt) || pool_layer_elems % per16 != 0 ||
       tree_layer_elems % per16 != 0 || (n_layers > 1 && (pool_layer_elems == 0 || tree_layer_elems == 0)))
     return MEDUSA_ERR_INVALID_ARG;
-  const PagedKV pg{0, page_rows, block_table, Kt, Vt};
+  // pages in one layer's pool; a page id at or beyond it is never written (unknown when the
+  // caller passes no layer size for a single layer)
+  const size_t page_elems = (size_t)cfg->Hkv * page_rows * cfg->D;
+  const size_t pages = pool_layer_elems ? pool_layer_elems / page_elems : (size_t)INT32_MAX;
+  const PagedKV pg{(int)(pages < (size_t)INT32_MAX ? pages : (size_t)INT32_MAX), page_rows, block_table, Kt, Vt};
   return from_cuda(launch_kv_commit_paged(*cfg, Kp, Vp, pg, n_layers, pool_layer_elems, tree_layer_elems, L, acc, path,
                                           kv_map, (cudaStream_t)stream));
 }
@@ -285,6 +289,28 @@ int medusa_poll_errors(medusa_stream_t stream, uint32_t* heads_codes, uint32_t* 
   return (h | a) ? MEDUSA_ERR_TIMEOUT : MEDUSA_OK;
 }
 
+int medusa_checked_build(void) {
+#ifdef MEDUSA_CHECKED
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int medusa_poll_checks(medusa_stream_t stream, uint32_t* codes) {
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t w[4] = {0, 0, 0, 0};
+  cudaError_t e = tree_take_checks(&w[0], st);
+  if (e == cudaSuccess) e = verify_take_checks(&w[1], st);
+  if (e == cudaSuccess) e = compact_take_checks(&w[2], st);
+  if (e == cudaSuccess) e = attention_tc_take_checks(&w[3], st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return MEDUSA_ERR_CUDA;
+  const uint32_t all = w[0] | w[1] | w[2] | w[3];
+  if (codes) *codes = all;
+  return all ? MEDUSA_ERR_BOUNDS : MEDUSA_OK;
+}
+
 int medusa_selftest_wait_timeout(uint32_t budget_us, medusa_stream_t stream) {
   if (budget_us < 1 || budget_us > 1000000) return MEDUSA_ERR_INVALID_ARG;
   return from_cuda(launch_wait_selftest((long long)budget_us * 2100, (cudaStream_t)stream));   // <= 2.1 GHz SM clock
@@ -300,6 +326,7 @@ const char* medusa_status_string(int status) {
     case MEDUSA_ERR_CAPACITY: return "KV cache capacity exceeded";
     case MEDUSA_ERR_CUDA: return "CUDA launch error";
     case MEDUSA_ERR_TIMEOUT: return "device wait timed out";
+    case MEDUSA_ERR_BOUNDS: return "out-of-range index met on the device (checked build)";
     default: return "unknown status";
   }
 }

@@ -173,7 +173,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     const uint16_t* __restrict__ Q, const int32_t* __restrict__ L, const uint64_t* __restrict__ bits,
                     int N, int Hq, int Hkv, int L_cap, int chunk, float scale_log2, float* __restrict__ o_part,
                     float* __restrict__ ml_part, uint16_t* __restrict__ O, const int32_t* __restrict__ block_table,
-                    int page_rows, float* __restrict__ x_part) {
+                    int page_rows, int num_pages, float* __restrict__ x_part) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
@@ -346,6 +346,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         page_reg = jj < ptiles ? block_table[(size_t)b * max_pages + (k_begin + jj * kKeys) / page_rows] : 0;
       }
       const int page = __shfl_sync(0xffffffffu, page_reg, j & 31);
+      // a page id outside the pool addresses rows past the tensor map, which TMA fills with zeros
+      MEDUSA_CHECK(tree || lane != 0 || (page >= 0 && page < num_pages), MEDUSA_CHECK_PAGE);
       const int key0 = k_begin + j * kKeys;
       const int row0 = tree ? (b * Hkv + kvh) * N : (page * Hkv + kvh) * page_rows + key0 % page_rows;
       if (lane == 0) {
@@ -831,6 +833,8 @@ bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+MEDUSA_CHECK_TAKE(attention_tc_take_checks)
+
 // Q-tile CTAs per (sequence, KV head): a short remainder of rows rides with the full tiles' CTAs.
 cudaError_t attention_tc_take_error(uint32_t* out, cudaStream_t st) {
   static const uint32_t zero = 0;
@@ -897,7 +901,8 @@ cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, cons
   dim3 grid(attention_tc_mtiles(NG), c.Hkv * c.B, nsplit);
   launch_pdl(kernel, grid, threads_of(fold), smem_of(fold), st, tmK, tmV, tmKt, tmVt, static_cast<const uint16_t*>(Q),
              L, bits, ts.N, c.Hq, c.Hkv, c.L_cap, chunk, scale_log2, o_part, ml_part, static_cast<uint16_t*>(O),
-             paged ? paged->block_table : static_cast<const int32_t*>(nullptr), paged ? paged->page_rows : 0, x_part);
+             paged ? paged->block_table : static_cast<const int32_t*>(nullptr), paged ? paged->page_rows : 0,
+             paged ? paged->num_pages : 0, x_part);
   note_launches(1);
   return cudaGetLastError();
 }

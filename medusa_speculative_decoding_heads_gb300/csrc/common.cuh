@@ -169,6 +169,44 @@ cudaError_t launch_kv_compact(const medusa_cfg& c, void* Kc, void* Vc, int32_t* 
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Checked build (-DMEDUSA_CHECKED). Where a kernel meets an index it read from
+// device memory (a token id, a tree link, a path node, a page id) outside the
+// range it may address, it already clamps the index or skips the access; the
+// checked build also ORs a MEDUSA_CHECK_* code into a device word of the
+// translation unit, which medusa_poll_checks reads and clears. Nothing traps.
+// In the normal build MEDUSA_CHECK compiles to nothing.
+#ifdef MEDUSA_CHECKED
+namespace {
+__device__ uint32_t g_check_word = 0;
+}
+#define MEDUSA_CHECK(cond, code)                                  \
+  do {                                                            \
+    if (!(cond)) atomicOr(&::medusa::g_check_word, (uint32_t)(code)); \
+  } while (0)
+// Defines `cudaError_t fn(uint32_t* out, cudaStream_t st)`: stream-ordered read-and-clear of
+// this translation unit's check word (the caller synchronises before reading *out).
+#define MEDUSA_CHECK_TAKE(fn)                                                                                \
+  cudaError_t fn(uint32_t* out, cudaStream_t st) {                                                          \
+    static const uint32_t zero = 0;                                                                         \
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_check_word, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, st); \
+    if (e != cudaSuccess) return e;                                                                         \
+    return cudaMemcpyToSymbolAsync(g_check_word, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, st);  \
+  }
+#else
+#define MEDUSA_CHECK(cond, code) \
+  do {                           \
+  } while (0)
+#define MEDUSA_CHECK_TAKE(fn)                              \
+  cudaError_t fn(uint32_t* out, cudaStream_t) {            \
+    *out = 0;                                              \
+    return cudaSuccess;                                    \
+  }
+#endif
+cudaError_t tree_take_checks(uint32_t* out, cudaStream_t st);
+cudaError_t verify_take_checks(uint32_t* out, cudaStream_t st);
+cudaError_t compact_take_checks(uint32_t* out, cudaStream_t st);
+cudaError_t attention_tc_take_checks(uint32_t* out, cudaStream_t st);
+
 // Configuration checks shared by every entry point (MEDUSA_OK or an error status).
 int check_cfg_public(const medusa_cfg* c);
 

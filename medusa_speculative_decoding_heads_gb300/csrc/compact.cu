@@ -24,6 +24,14 @@ __device__ __forceinline__ bool valid_walk(int Lb, int N, int L_cap, int a, int 
   return Lb >= 0 && Lb + N <= L_cap && a >= 0 && a <= K;
 }
 
+// Path slot r holds a node of the tree, the root at r = 0 and a deeper node
+// than slot r - 1 after it (so node ids grow strictly and slot r's node is at
+// least r, which the in-place move relies on).
+__device__ __forceinline__ bool path_node_ok(const int32_t* pb, int r, int N) {
+  const int s = pb[r];
+  return s >= 0 && s < N && (r == 0 ? s == 0 : s > pb[r - 1]);
+}
+
 __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -46,11 +54,13 @@ kv_compact_kernel(uint4* __restrict__ Kc, uint4* __restrict__ Vc, int Hkv, int r
   const int a = acc[b];
   const bool ok = valid_walk(Lb, N, L_cap, a, K);
   const int32_t* pb = path + (size_t)b * (K + 1);
+  MEDUSA_CHECK(!(Lb >= 0 && Lb + N <= L_cap) || (a >= 0 && a <= K), MEDUSA_CHECK_PATH);
   if (ok) {
     int src[kMaxK + 1];
 #pragma unroll
     for (int r = 0; r <= kMaxK; ++r) {
       const int s = r <= a ? pb[r] : r;
+      MEDUSA_CHECK(r > a || path_node_ok(pb, r, N), MEDUSA_CHECK_PATH);
       src[r] = s < 0 ? 0 : (s >= N ? N - 1 : s);
     }
     const int h0 = rank * Hkv / ncta, h1 = (rank + 1) * Hkv / ncta;
@@ -84,7 +94,8 @@ kv_compact_kernel(uint4* __restrict__ Kc, uint4* __restrict__ Vc, int Hkv, int r
 __global__ void __launch_bounds__(kCompactThreads)
 kv_commit_paged_kernel(uint4* __restrict__ Kp, uint4* __restrict__ Vp, const uint4* __restrict__ Kt,
                        const uint4* __restrict__ Vt, const int32_t* __restrict__ block_table, int max_pages,
-                       int page_rows, int n_layers, size_t pool_layer_vec, size_t tree_layer_vec, int Hkv, int row_vec,
+                       int num_pages, int page_rows, int n_layers, size_t pool_layer_vec, size_t tree_layer_vec,
+                       int Hkv, int row_vec,
                        int N, int K, int32_t* __restrict__ L, const int32_t* __restrict__ acc,
                        const int32_t* __restrict__ path, int32_t* __restrict__ kv_map) {
   pdl_wait();
@@ -94,15 +105,22 @@ kv_commit_paged_kernel(uint4* __restrict__ Kp, uint4* __restrict__ Vp, const uin
   const int a = acc[b];
   const bool ok = Lb >= 0 && Lb + N <= max_pages * page_rows && a >= 0 && a <= K;
   const int32_t* pb = path + (size_t)b * (K + 1);
+  MEDUSA_CHECK(!(Lb >= 0 && Lb + N <= max_pages * page_rows) || (a >= 0 && a <= K), MEDUSA_CHECK_PATH);
   if (ok) {
     int src[kMaxK + 1];
     size_t dst[kMaxK + 1];   // pool row of logical row Lb + r, before the head offset
+    bool live[kMaxK + 1];    // r <= acc and the row's page lies inside the pool
 #pragma unroll
     for (int r = 0; r <= kMaxK; ++r) {
       const int sr = r <= a ? pb[r] : 0;
+      MEDUSA_CHECK(r > a || path_node_ok(pb, r, N), MEDUSA_CHECK_PATH);
       src[r] = sr < 0 ? 0 : (sr >= N ? N - 1 : sr);
       const int row = Lb + (r <= a ? r : 0);
-      dst[r] = (size_t)block_table[(size_t)b * max_pages + row / page_rows] * Hkv * page_rows + row % page_rows;
+      const int page = block_table[(size_t)b * max_pages + row / page_rows];
+      const bool in_pool = page >= 0 && page < num_pages;
+      MEDUSA_CHECK(r > a || in_pool, MEDUSA_CHECK_PAGE);
+      live[r] = r <= a && in_pool;   // a page id outside the pool: that row is not written
+      dst[r] = (size_t)(in_pool ? page : 0) * Hkv * page_rows + row % page_rows;
     }
     const int pairs = n_layers * Hkv * 2;              // (layer, head, K or V)
     for (int i = rank * kCompactThreads + threadIdx.x; i < pairs * row_vec; i += ncta * kCompactThreads) {
@@ -112,7 +130,7 @@ kv_commit_paged_kernel(uint4* __restrict__ Kp, uint4* __restrict__ Vp, const uin
       uint4* dbase = (kv ? Vp : Kp) + layer * pool_layer_vec + (size_t)h * page_rows * row_vec + col;
 #pragma unroll
       for (int r = 0; r <= kMaxK; ++r)
-        if (r <= a) dbase[dst[r] * row_vec] = sbase[(size_t)src[r] * row_vec];
+        if (live[r]) dbase[dst[r] * row_vec] = sbase[(size_t)src[r] * row_vec];
     }
   }
   cluster_barrier();
@@ -124,6 +142,8 @@ kv_commit_paged_kernel(uint4* __restrict__ Kp, uint4* __restrict__ Vp, const uin
 }
 
 }  // namespace
+
+MEDUSA_CHECK_TAKE(compact_take_checks)
 
 cudaError_t launch_kv_compact(const medusa_cfg& c, void* Kc, void* Vc, int32_t* L, const int32_t* acc,
                               const int32_t* path, int32_t* kv_map, cudaStream_t st) {
@@ -177,7 +197,7 @@ cudaError_t launch_kv_commit_paged(const medusa_cfg& c, void* Kp, void* Vp, cons
   cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kv_commit_paged_kernel, static_cast<uint4*>(Kp), static_cast<uint4*>(Vp),
                                      static_cast<const uint4*>(pg.Kt), static_cast<const uint4*>(pg.Vt), pg.block_table,
-                                     c.L_cap / pg.page_rows, pg.page_rows, n_layers, pool_layer_elems / per16,
+                                     c.L_cap / pg.page_rows, pg.num_pages, pg.page_rows, n_layers, pool_layer_elems / per16,
                                      tree_layer_elems / per16, c.Hkv, row_vec, ts.N, c.K, L, acc, path, kv_map);
   note_launches(1);
   if (e != cudaSuccess) return e;

@@ -44,7 +44,7 @@ struct TreeNodes {
 };
 
 __global__ void __launch_bounds__(kMaxN)
-tree_build_kernel(TreeShape ts, TreeNodes tn, int B, int L_cap, const int32_t* __restrict__ root,
+tree_build_kernel(TreeShape ts, TreeNodes tn, int B, int L_cap, int V, const int32_t* __restrict__ root,
                   const int32_t* __restrict__ topk,
                   const int32_t* __restrict__ L, int32_t* __restrict__ parent, int32_t* __restrict__ depth,
                   int32_t* __restrict__ first_child, uint8_t* __restrict__ mask, uint64_t* __restrict__ bits,
@@ -75,7 +75,9 @@ tree_build_kernel(TreeShape ts, TreeNodes tn, int B, int L_cap, const int32_t* _
     }
   }
   if (n < N) {
-    tokens[(size_t)b * N + n] = d == 0 ? root[b] : topk[((size_t)b * ts.K + (d - 1)) * ts.s_max + rank];
+    const int tok = d == 0 ? root[b] : topk[((size_t)b * ts.K + (d - 1)) * ts.s_max + rank];
+    MEDUSA_CHECK(tok >= 0 && tok < V, MEDUSA_CHECK_TOKEN);
+    tokens[(size_t)b * N + n] = tok;
     pos[(size_t)b * N + n] = Lb + d;
   }
   if (b != 0) return;   // the tree arrays are the same for every sequence: block 0 writes them
@@ -103,6 +105,8 @@ tree_build_kernel(TreeShape ts, TreeNodes tn, int B, int L_cap, const int32_t* _
 
 }  // namespace
 
+MEDUSA_CHECK_TAKE(tree_take_checks)
+
 cudaError_t launch_tree_build(const medusa_cfg& c, const int32_t* root, const int32_t* topk, const int32_t* L,
                               int32_t* parent, int32_t* depth, int32_t* first_child, uint8_t* mask, uint64_t* bits,
                               int32_t* tokens, int32_t* pos, uint32_t* flags, cudaStream_t st) {
@@ -113,7 +117,7 @@ cudaError_t launch_tree_build(const medusa_cfg& c, const int32_t* root, const in
       tn.parent[n] = c.tree_parent[n];
       tn.rank[n] = c.tree_rank[n];
     }
-  launch_pdl(tree_build_kernel, c.B, kMaxN, 0, st, ts, tn, c.B, c.L_cap, root, topk, L, parent, depth, first_child, mask,
+  launch_pdl(tree_build_kernel, c.B, kMaxN, 0, st, ts, tn, c.B, c.L_cap, c.V, root, topk, L, parent, depth, first_child, mask,
              bits, tokens, pos, flags);
   note_launches(1);
   return cudaGetLastError();

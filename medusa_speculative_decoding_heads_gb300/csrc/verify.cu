@@ -230,6 +230,13 @@ struct WalkOut {
 // thread 0 looks for the child carrying that token among the node's children
 // (held in shared memory with the sequence's tokens) and the CTA descends or
 // stops. Rows the walk does not reach are never read.
+// The links a walk follows: the root has no parent, every other node's parent
+// comes before it, and a first child (if any) comes after its node. The walks
+// only follow links that stay inside the tree, whatever these arrays hold.
+__device__ __forceinline__ bool tree_links_ok(int i, int N, int par, int fc) {
+  return (i == 0 ? par == -1 : (par >= 0 && par < i)) && (fc == -1 || (fc > i && fc < N));
+}
+
 constexpr int kGwThreads = 512;
 constexpr int kGwWarps = kGwThreads / 32;
 
@@ -248,6 +255,7 @@ greedy_walk_kernel(TreeShape ts, int V, const int32_t* __restrict__ tokens, cons
     s_tok[i] = tokens[(size_t)b * N + i];
     s_par[i] = parent[i];
     s_fc[i] = first_child[i];
+    MEDUSA_CHECK(tree_links_ok(i, N, s_par[i], s_fc[i]), MEDUSA_CHECK_TREE);
   }
   int32_t* path = w.path + (size_t)b * (K + 1);
   int32_t* out = w.out_tokens + (size_t)b * (K + 1);
@@ -749,6 +757,7 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
     s_tok[i] = tokens[(size_t)b * N + i];
     s_fc[i] = first_child[i];
     s_par[i] = parent[i];
+    MEDUSA_CHECK(tree_links_ok(i, N, s_par[i], s_fc[i]), MEDUSA_CHECK_TREE);
   }
   uint32_t fl = 0;
   int xn = 0;
@@ -776,7 +785,9 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
     if (fetch) {
       const int fc = s_fc[cur];
       const int j = threadIdx.x;
-      const int xt = (fc >= 0 && fc + j < N && s_par[fc + j] == cur) ? min(max(s_tok[fc + j], 0), V - 1) : 0;
+      const bool child = fc >= 0 && fc + j < N && s_par[fc + j] == cur;
+      MEDUSA_CHECK(!child || (s_tok[fc + j] >= 0 && s_tok[fc + j] < V), MEDUSA_CHECK_TOKEN);
+      const int xt = child ? min(max(s_tok[fc + j], 0), V - 1) : 0;
       ct = Elt<T>::load(trow, xt);
       ch = hl[((size_t)b * K + (dep - 1)) * V + xt];
       cu = u_acc[((size_t)b * K + (dep - 1)) * ts.s_max + j];
@@ -996,6 +1007,8 @@ cudaError_t run_greedy(const medusa_cfg& c, const TreeShape& ts, const int32_t* 
 }
 
 }  // namespace
+
+MEDUSA_CHECK_TAKE(verify_take_checks)
 
 size_t verify_workspace(const medusa_cfg& c) {
   const TreeShape ts = tree_shape(c);
