@@ -6,9 +6,14 @@
 // the running maximum and exp-sum ("최적화 2편" (beengineer500), section 3.3).
 //
 // One CTA = one 128-row Q tile (tree nodes x query heads of one KV head) against
-// one KV range of one sequence, in tiles of 128 keys. 19 warps (23 with leftover rows):
-//   warp 16 TMA producer: K and V tiles (two 64-column boxes each, 128-byte
-//           swizzle) into a 3-stage ring; allocates TMEM.
+// one KV range of one sequence, in tiles of 128 keys. 20 warps (24 with leftover rows):
+//   warp 16 TMA producer of K tiles (two 64-column boxes, 128-byte swizzle) into a
+//           3-stage K ring; a K stage is free again as soon as S_j (and S'_j) has
+//           read it. Allocates TMEM.
+//   warp 19 (23 with leftover rows) TMA producer of V tiles into a 3-stage V ring;
+//           a V stage is free again once PV_j (and PV'_j) has read it. With K and V
+//           in rings of their own, no stage stays held across the softmax, so
+//           more of the shared memory holds loads in flight.
 //   warp 17 S issuer: S_j = Q K_j^T (Q held in TMEM, K from shared memory) into
 //           one of two S tiles in TMEM, so that S_{j+1} is computed while the
 //           softmax works on S_j.
@@ -54,8 +59,14 @@ constexpr int kRows = 128;                  // query rows per Q tile (MMA M)
 constexpr int kD = 128;
 constexpr int kHalf = 128 * 128;            // 128 rows x 64 bf16: one 128-byte-swizzled half of a tile (16 KB)
 constexpr int kOperand = 2 * kHalf;         // a 128 x 128 bf16 tile, K or V (32 KB)
-constexpr int kStage = 2 * kOperand;        // K + V of one key tile
-constexpr int kStages = 3;
+#ifndef MEDUSA_ATTN_KSTAGES
+#define MEDUSA_ATTN_KSTAGES 3
+#endif
+#ifndef MEDUSA_ATTN_VSTAGES
+#define MEDUSA_ATTN_VSTAGES 3
+#endif
+constexpr int kStagesK = MEDUSA_ATTN_KSTAGES;   // stages of the K ring
+constexpr int kStagesV = MEDUSA_ATTN_VSTAGES;   // stages of the V ring
 constexpr int kGroups = 4;                  // softmax warpgroups, 32 keys each
 constexpr int kXchg = kGroups * kRows * 4;   // exp-sums [group][row] for the epilogue (2 KB)
 constexpr int kXRows = 16;                   // N of the narrow products (the smallest N with M = 128)
@@ -63,7 +74,8 @@ constexpr int kXMax = 8;                     // leftover query rows one CTA carr
 constexpr int kXHalf = kXRows * 128;         // 16 rows x 64 bf16, one 128-byte-swizzled half (2 KB)
 // shared memory: K/V ring | exp-sums | and with leftover rows: Q' [16 rows][128 dims] | P' two slots
 // [16 rows][128 keys] | their reductions (maxima [2][4 warps][16], sums [4 warps][16])
-constexpr int kOffXl = kStages * kStage;
+constexpr int kOffV = kStagesK * kOperand;   // the V ring follows the K ring
+constexpr int kOffXl = (kStagesK + kStagesV) * kOperand;
 constexpr int kOffQx = kOffXl + kXchg;   // 1024-byte aligned, as the swizzled operands need
 constexpr int kOffPx = kOffQx + 2 * kXHalf;
 constexpr int kOffRed = kOffPx + 4 * kXHalf;
@@ -75,8 +87,9 @@ constexpr int kProducerWarp = 16;
 constexpr int kMmaSWarp = 17;   // issues S = Q K^T (and S'^T = K Q'^T)
 constexpr int kMmaPWarp = 18;   // issues O += P V (and O'^T += V^T P'^T)
 constexpr int kXWarp0 = 19;     // warps 19-22: softmax of the leftover rows
-// 19 warps; 23 for configurations whose query rows per KV head end in a short remainder
-__host__ __device__ constexpr int threads_of(bool fold) { return (fold ? 23 : 19) * 32; }
+__host__ __device__ constexpr int vproducer_warp(bool fold) { return fold ? 23 : 19; }
+// 20 warps; 24 for configurations whose query rows per KV head end in a short remainder
+__host__ __device__ constexpr int threads_of(bool fold) { return (vproducer_warp(fold) + 1) * 32; }
 constexpr int kSortMax = 256;   // batches up to this size are taken longest sequence first
 
 // TMEM columns: two S tiles (128 f32 columns each; warpgroup q writes P of its
@@ -178,9 +191,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring = sm;                                                    // [stage][K | V]
+  uint8_t* ring = sm;                                                    // K ring [stage], then V ring [stage]
   float* xl = reinterpret_cast<float*>(sm + kOffXl);   // [group][row] exp-sums
-  __shared__ __align__(8) uint64_t kv_full[kStages], kv_empty[kStages], s_full[2], p_full[2], p_free[2], xbar;
+  __shared__ __align__(8) uint64_t k_full[kStagesK], k_empty[kStagesK], v_full[kStagesV], v_empty[kStagesV];
+  __shared__ __align__(8) uint64_t s_full[2], p_full[2], p_free[2], xbar;
   __shared__ __align__(8) uint64_t s2_full[2], p2_full[2], p2_free[2], xbar2;   // leftover rows
   __shared__ uint32_t tmem_slot;
   __shared__ int seq;
@@ -265,9 +279,13 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   }
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      tc::mbar_init(&kv_full[i], 1);
-      tc::mbar_init(&kv_empty[i], 1);
+    for (int i = 0; i < kStagesK; ++i) {
+      tc::mbar_init(&k_full[i], 1);
+      tc::mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < kStagesV; ++i) {
+      tc::mbar_init(&v_full[i], 1);
+      tc::mbar_init(&v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&s_full[i], 1);
@@ -326,67 +344,58 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   __syncthreads();
   tc::fence_after();
 
-  if (warp == kProducerWarp && page_rows > 0) {
-    // ---------------------------------------------------------- TMA producer, paged
-    // Prefix tile j (keys k_begin + 128 j ..) lies inside one page (page_rows is a
-    // multiple of 128): pool row (page * Hkv + kvh) * page_rows + key % page_rows.
-    // The tree tile comes from the staging buffer, row (b * Hkv + kvh) * N. The
-    // whole warp walks the schedule: every 32 tiles each lane fetches one block-table
-    // entry and lane 0 takes them by shuffle.
-    const int max_pages = L_cap / page_rows;
+  if (warp == kProducerWarp || warp == vproducer_warp(kFold)) {
+    // ------------------------------------------------------------ TMA producers
+    // Warp 16 loads the K tiles, the V producer warp the V tiles, each into its own
+    // ring, waiting only for its own ring's stages. Paged cache: prefix tile j
+    // (keys k_begin + 128 j ..) lies inside one page (page_rows is a multiple of
+    // 128), pool row (page * Hkv + kvh) * page_rows + key % page_rows; every 32
+    // tiles each lane fetches one block-table entry and lane 0 takes them by
+    // shuffle. The tree tile comes from the staging buffer, row (b * Hkv + kvh) * N.
+    // Contiguous cache: row (b * Hkv + kvh) * L_cap + key.
+    const bool isv = warp != kProducerWarp;
+    uint64_t* full = isv ? v_full : k_full;
+    uint64_t* empty = isv ? v_empty : k_empty;
+    uint8_t* base = ring + (isv ? kOffV : 0);
+    const CUtensorMap* mp = isv ? &tmV : &tmK;     // prefix rows
+    const CUtensorMap* mt_ = isv ? &tmVt : &tmKt;  // tree rows (the same map unless paged)
+    const int nst = isv ? kStagesV : kStagesK;
+    const int max_pages = page_rows > 0 ? L_cap / page_rows : 0;
+    const int head_row = (b * Hkv + kvh) * L_cap;
     int page_reg = 0, issued = 0;
     for (int j = 0; j < ntiles; ++j) {
-      const int st = j % kStages;
+      const int st = j % nst;
       bool ok = true;
-      if (j >= kStages) ok = tc::mbar_wait<true>(&kv_empty[st], ((j / kStages) - 1) & 1, err, 1);
+      if (j >= nst) ok = tc::mbar_wait<true>(&empty[st], ((j / nst) - 1) & 1, err, 1);
       if (!__all_sync(0xffffffffu, ok)) break;
       const bool tree = j >= ptiles;
-      if (!tree && (j & 31) == 0) {
-        const int jj = j + lane;
-        page_reg = jj < ptiles ? block_table[(size_t)b * max_pages + (k_begin + jj * kKeys) / page_rows] : 0;
+      int row0;
+      if (page_rows > 0) {
+        if (!tree && (j & 31) == 0) {
+          const int jj = j + lane;
+          page_reg = jj < ptiles ? block_table[(size_t)b * max_pages + (k_begin + jj * kKeys) / page_rows] : 0;
+        }
+        const int page = __shfl_sync(0xffffffffu, page_reg, j & 31);
+        // a page id outside the pool addresses rows past the tensor map, which TMA fills with zeros
+        MEDUSA_CHECK(isv || tree || lane != 0 || (page >= 0 && page < num_pages), MEDUSA_CHECK_PAGE);
+        const int key0 = k_begin + j * kKeys;
+        row0 = tree ? (b * Hkv + kvh) * N : (page * Hkv + kvh) * page_rows + key0 % page_rows;
+      } else {
+        row0 = tree ? head_row + Lb : head_row + k_begin + j * kKeys;
       }
-      const int page = __shfl_sync(0xffffffffu, page_reg, j & 31);
-      // a page id outside the pool addresses rows past the tensor map, which TMA fills with zeros
-      MEDUSA_CHECK(tree || lane != 0 || (page >= 0 && page < num_pages), MEDUSA_CHECK_PAGE);
-      const int key0 = k_begin + j * kKeys;
-      const int row0 = tree ? (b * Hkv + kvh) * N : (page * Hkv + kvh) * page_rows + key0 % page_rows;
       if (lane == 0) {
-        const CUtensorMap* mk = tree ? &tmKt : &tmK;
-        const CUtensorMap* mv = tree ? &tmVt : &tmV;
-        uint8_t* dst = ring + st * kStage;
-        tc::mbar_arrive_expect(&kv_full[st], kStage);
-        tc::tma_load_2d(dst, mk, 0, row0, &kv_full[st]);
-        tc::tma_load_2d(dst + kHalf, mk, 64, row0, &kv_full[st]);
-        tc::tma_load_2d(dst + kOperand, mv, 0, row0, &kv_full[st]);
-        tc::tma_load_2d(dst + kOperand + kHalf, mv, 64, row0, &kv_full[st]);
+        const CUtensorMap* m = tree ? mt_ : mp;
+        uint8_t* dst = base + st * kOperand;
+        tc::mbar_arrive_expect(&full[st], kOperand);
+        tc::tma_load_2d(dst, m, 0, row0, &full[st]);
+        tc::tma_load_2d(dst + kHalf, m, 64, row0, &full[st]);
       }
       __syncwarp();
       issued = j + 1;
     }
     if (lane == 0)   // drain: never leave the CTA with tile loads still landing in shared memory
-      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
-        tc::mbar_wait(&kv_full[j % kStages], (j / kStages) & 1, err, 128);
-  } else if (warp == kProducerWarp) {
-    if (lane == 0) {
-      // ---------------------------------------------------------------- TMA producer
-      const int head_row = (b * Hkv + kvh) * L_cap;
-      int issued = 0;
-      for (int j = 0; j < ntiles; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages && !tc::mbar_wait<true>(&kv_empty[st], ((j / kStages) - 1) & 1, err, 1)) break;
-        const int row0 = j < ptiles ? head_row + k_begin + j * kKeys : head_row + Lb;
-        uint8_t* dst = ring + st * kStage;
-        tc::mbar_arrive_expect(&kv_full[st], kStage);
-        tc::tma_load_2d(dst, &tmK, 0, row0, &kv_full[st]);
-        tc::tma_load_2d(dst + kHalf, &tmK, 64, row0, &kv_full[st]);
-        tc::tma_load_2d(dst + kOperand, &tmV, 0, row0, &kv_full[st]);
-        tc::tma_load_2d(dst + kOperand + kHalf, &tmV, 64, row0, &kv_full[st]);
-        issued = j + 1;
-      }
-      // Drain: never leave the CTA with tile loads still landing in shared memory.
-      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
-        tc::mbar_wait(&kv_full[j % kStages], (j / kStages) & 1, err, 128);
-    }
+      for (int j = issued > nst ? issued - nst : 0; j < issued; ++j)
+        tc::mbar_wait(&full[j % nst], (j / nst) & 1, err, 128);
   } else if (warp == kMmaSWarp) {
     // ------------------------------------------------------------------ S issuer
     // The whole warp walks the schedule (uniform waits); one elected lane issues.
@@ -395,14 +404,14 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     const uint64_t dK = tc::sw128_desc(tc::saddr(ring), 16, 1024);
     const uint64_t dQx = tc::sw128_desc(tc::saddr(sm + kOffQx), 16, 1024);
     for (int j = 0; j < ntiles; ++j) {
-      const int slot = j & 1, st = j % kStages;
-      bool ok = tc::mbar_wait<true>(&kv_full[st], (j / kStages) & 1, err, 2);
+      const int slot = j & 1, st = j % kStagesK;
+      bool ok = tc::mbar_wait<true>(&k_full[st], (j / kStagesK) & 1, err, 2);
       // S tile `slot` still holds P_{j-2} until PV_{j-2} completes
       if (ok && j >= 2) ok = tc::mbar_wait<true>(&p_free[slot], ((j >> 1) - 1) & 1, err, 4);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc::fence_after();
       if (tc::elect_one()) {
-        const uint64_t b0 = dK + (uint64_t)((st * kStage) >> 4);
+        const uint64_t b0 = dK + (uint64_t)((st * kOperand) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
@@ -419,7 +428,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           break;
         tc::fence_after();
         if (tc::elect_one()) {
-          const uint64_t a0 = dK + (uint64_t)((st * kStage) >> 4);
+          const uint64_t a0 = dK + (uint64_t)((st * kOperand) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
@@ -430,14 +439,16 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         }
         __syncwarp();
       }
+      // the K stage is free once this tile's S (and S') products have read it
+      if (tc::elect_one()) tc::commit(&k_empty[st]);
+      __syncwarp();
     }
   } else if (warp == kMmaPWarp) {
     // ------------------------------------------------------------------ PV issuer
-    // S_j completed before P_j was released, so the completion of PV_j also
-    // covers every read of the stage's K tile.
+    // The completion of PV_j (and of PV'_j on a tile with leftover rows) frees V stage j.
     constexpr uint32_t idPV = tc::idesc_bf16_f32(kRows, kD, 0, 1);
     constexpr uint32_t idPV2 = tc::idesc_bf16_f32(kD, kXRows, 1, 0);   // A = V^T (MN-major), B = P' (K-major)
-    const uint64_t dV = tc::sw128_desc(tc::saddr(ring + kOperand), kHalf, 1024);   // MN-major: LBO = 64-column half
+    const uint64_t dV = tc::sw128_desc(tc::saddr(ring + kOffV), kHalf, 1024);   // MN-major: LBO = 64-column half
     const uint64_t dPx = tc::sw128_desc(tc::saddr(sm + kOffPx), 16, 1024);
     // O'^T += V_t^T P'^T for narrow tile jx (key tile t) once its leftover softmax has arrived;
     // its completion also frees the stage
@@ -445,7 +456,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       if (!__all_sync(0xffffffffu, tc::mbar_wait<true>(&p2_full[jx & 1], (jx >> 1) & 1, err, 2048))) return false;
       tc::fence_after();
       if (tc::elect_one()) {
-        const uint64_t a0 = dV + (uint64_t)(((t % kStages) * kStage) >> 4);
+        const uint64_t a0 = dV + (uint64_t)(((t % kStagesV) * kOperand) >> 4);
         const uint64_t p0 = dPx + (uint64_t)(((jx & 1) * 2 * kXHalf) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
@@ -453,24 +464,25 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           tc::mma_bf16(tmem + kColO2, a0 + (uint64_t)((kk * 2048) >> 4), p0 + offx, idPV2, (jx > 0 || kk > 0) ? 1 : 0);
         }
         tc::commit(&p2_free[jx & 1]);
-        tc::commit(&kv_empty[t % kStages]);
+        tc::commit(&v_empty[t % kStagesV]);
       }
       __syncwarp();
       return true;
     };
     for (int j = 0; j < ntiles; ++j) {
-      const int slot = j & 1, st = j % kStages;
-      const bool ok = tc::mbar_wait<true>(&p_full[slot], (j >> 1) & 1, err, 8);
+      const int slot = j & 1, st = j % kStagesV;
+      bool ok = tc::mbar_wait<true>(&v_full[st], (j / kStagesV) & 1, err, 1u << 17);
+      if (ok) ok = tc::mbar_wait<true>(&p_full[slot], (j >> 1) & 1, err, 8);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc::fence_after();
       if (tc::elect_one()) {
-        const uint64_t b0 = dV + (uint64_t)((st * kStage) >> 4);
+        const uint64_t b0 = dV + (uint64_t)((st * kOperand) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)   // keys [16kk, 16kk + 16): group kk / 2, P columns 32(kk/2) + 8(kk%2)
           tc::mma_bf16_tmem_a(tmem + kColO, tmem + col_S(slot) + 32 * (kk >> 1) + 8 * (kk & 1),
                               b0 + (uint64_t)((kk * 2048) >> 4), idPV, (j > 0 || kk > 0) ? 1 : 0);
         tc::commit(&p_free[slot]);
-        if (!(xtra && j % MT == mt)) tc::commit(&kv_empty[st]);
+        if (!(xtra && j % MT == mt)) tc::commit(&v_empty[st]);
       }
       __syncwarp();
       if (xtra && j % MT == mt && !issue_pv2(j, j / MT)) break;
