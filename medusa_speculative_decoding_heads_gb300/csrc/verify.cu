@@ -959,10 +959,14 @@ cudaError_t launch_rs_walk(const medusa_cfg& c, const TreeShape& ts, int ncta, i
 
 // CTAs per sequence: the largest power of two (at most 8) that keeps the whole
 // grid within one CTA per SM (eight per sequence at B = 32 measured no faster
-// than four: the walk's time is its chain of cluster exchanges, not the slices).
-int rs_cluster_ctas(int B) {
+// than four: the walk's time is its chain of cluster exchanges, not the slices),
+// and at least enough that a CTA's slice fits the 32 entries per thread the walk
+// holds in registers (V <= 32768 needs at most 4; more CTAs than one wave is only
+// slower).
+int rs_cluster_ctas(int B, int V) {
   int n = 1;
   while (n < kMaxCluster && (long)B * n <= 152) n *= 2;
+  while (n < kMaxCluster && (long)n * 32 * kVThreads < V) n *= 2;
   return n;
 }
 
@@ -981,9 +985,10 @@ cudaError_t run_rs(const medusa_cfg& c, const TreeShape& ts, const int32_t* toke
   note_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int ncta = rs_cluster_ctas(c.B);
+  const int ncta = rs_cluster_ctas(c.B, c.V);
   const int slice = (((c.V + ncta - 1) / ncta) + 7) / 8 * 8;
   const int need = (slice + kVThreads - 1) / kVThreads;
+  if (need > 32) return cudaErrorInvalidValue;   // unreachable for V <= 32768 (checked by the entry point)
 #define MEDUSA_RS(CC) return launch_rs_walk<T, CC>(c, ts, ncta, slice, tokens, parent, first_child, tl, hl, stats, hsP, ua, ur, w, st)
   if (need <= 1) MEDUSA_RS(1);
   if (need <= 2) MEDUSA_RS(2);

@@ -397,9 +397,12 @@ def test_verify_rejection_decisions(name, T):
 
 
 # The walk runs on a cluster of 8 / 4 / 2 / 1 CTAs per sequence depending on B
-# (at most two 256-thread CTAs per SM); vocabulary slices of unequal length, rows
-# read 8 entries at a time or one at a time (V % 8 != 0).
-@pytest.mark.parametrize("B,V", [(8, 1000), (40, 4096), (80, 3001), (160, 2048)])
+# (one 256-thread CTA per SM), but on enough CTAs that each slice fits 32 entries
+# per thread (full vocabularies with large batches: more CTAs than one wave);
+# vocabulary slices of unequal length, rows read 8 entries at a time or one at a
+# time (V % 8 != 0).
+@pytest.mark.parametrize("B,V", [(8, 1000), (40, 4096), (80, 3001), (160, 2048), (40, 32000), (80, 32000),
+                                 (160, 32768), (24, 32000)])
 def test_verify_rejection_cluster_sizes(B, V):
     dev = gpu_ready()
     w = configs.scaled(configs.get("gqa7b_b32"), B=B, V=V, temperature=0.9, L_range=(16, 64))
