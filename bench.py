@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of one CUDA graph")
+    ap.add_argument("--fused", action="store_true",
+                    help="run each step as the one persistent kernel of medusa_step_fused (greedy, B <= 4)")
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed steps before the timed region")
     ap.add_argument("--paged", type=int, default=0,
                     help="with --part attention: rows per page of a shuffled paged pool (0: contiguous cache)")
@@ -422,6 +424,10 @@ def run_ours(args):
         lambda: st.kv_compact(inp.Kc, inp.Vc, inp.L),
     ]
     names = ["heads", "tree_build", "tree_attention", "verify", "kv_compact"]
+    if args.fused:   # the same step as one persistent kernel (a memset of its barrier word, then the launch)
+        fused_args = st.fused_args(inp, write_logits=False, compact=True)
+        calls = [lambda: mb.step_fused(st.cfg, fused_args, st.stream)]
+        names = ["fused_step"]
 
     def one_step(marks=None):
         inp.L.copy_(L0, non_blocking=True)
@@ -491,7 +497,7 @@ def run_ours(args):
     # run a little above ms_per_step)
     q = np.percentile([m[0].elapsed_time(m[-1]) for m in marks], [10, 50, 90])
     step_spread = {"p10": float(q[0]), "p50": float(q[1]), "p90": float(q[2]), "source": "event-marked replay"}
-    heads_ms = per_call["heads"]
+    heads_ms = per_call.get("heads", 0.0)
     elapsed_ms, value = replica_throughput(elapsed_ms, args.steps, world, dev)
     ms_per_step = elapsed_ms / args.steps
 
@@ -505,8 +511,11 @@ def run_ours(args):
     hbm, peak_kind = peaks()
     by = algorithmic_bytes(w, si.L, acc, mode, with_bias=si.bias is not None)
     heads_bytes = by["heads"] + (w.B * w.K * w.V * 4 if write_logits else 0)
-    attn_ms = per_call["tree_attention"]
-    if attn_ms > heads_ms:   # the dominant call is tree attention (long committed prefixes)
+    attn_ms = per_call.get("tree_attention", 0.0)
+    if args.fused:   # one kernel: the whole step's bytes over its duration
+        kernel = "medusa_step_fused (the whole step as one persistent kernel)"
+        dom_bytes, dom_ms, traffic = by["total"], per_call["fused_step"], None
+    elif attn_ms > heads_ms:   # the dominant call is tree attention (long committed prefixes)
         kernel = "medusa_tree_attention (tcgen05 tree attention over the committed KV)"
         dom_bytes, dom_ms, traffic = by["kv"] + by["tree_qkv"] + by["attn_out"], attn_ms, NCU_ATTN_TRAFFIC_BYTES.get(w.name)
     else:
@@ -530,7 +539,7 @@ def run_ours(args):
                           "bytes_by_term": by},
         "breakdown_ms": dict(per_call, step=ms_per_step),
         "marked_step_ms": step_spread,
-        "launch_mode": launch_mode,
+        "launch_mode": launch_mode + (", medusa_step_fused" if args.fused else ""),
         "accepted_per_step": float(np.mean(acc + 1)),
         "e2e": e2e,
     }
@@ -645,7 +654,10 @@ def run_e2e(w, st, inp, L0, tl, si, args, stream, world):
             else:
                 inp.Kc[b_idx, :, t_idx] = dv["tk"]
                 inp.Vc[b_idx, :, t_idx] = dv["tv"]
-            st.run(step_inp, write_logits=st.mode == REJECTION, compact=True)
+            if args.fused:
+                st.run_fused(step_inp, write_logits=False, compact=True)
+            else:
+                st.run(step_inp, write_logits=st.mode == REJECTION, compact=True)
             out_tok.copy_(st.out_tokens, non_blocking=True)
             freed[k % 2].record(cur)
         cur.wait_stream(copy_stream)

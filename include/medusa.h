@@ -238,6 +238,24 @@ MEDUSA_API int medusa_step_graph_create(const medusa_cfg* cfg, const medusa_step
 MEDUSA_API int medusa_step_graph_launch(medusa_step_graph* graph, medusa_stream_t stream);
 MEDUSA_API int medusa_step_graph_destroy(medusa_step_graph* graph);
 
+/* The whole step as one persistent kernel. Runs the five calls above (heads,
+ * tree, tree attention, greedy acceptance and, unless args->kv_compact is 0, KV
+ * compaction) as phases of a single cooperative launch with one CTA per SM; the
+ * phases meet at a grid-wide barrier whose every wait is bounded (an expired
+ * wait is recorded for medusa_poll_errors, as MEDUSA_FUSED_WAIT_CODE in its
+ * attention word; that call's outputs are then invalid). Buffers, layouts and
+ * results are those of the five calls ("Medusa 심층 아키텍처", section "트리
+ * 어텐션": all candidates verified in one forward pass); `logits` may be NULL.
+ * Supported: bf16, D = 128, MEDUSA_GREEDY, B <= 4 and B * d * 4 <= 200 KB
+ * (MEDUSA_ERR_UNSUPPORTED otherwise, nothing enqueued); h, W, bias, U, Q, Kc,
+ * Vc, O and target_logits 16-byte aligned (MEDUSA_ERR_INVALID_ARG otherwise).
+ * The weight GEMVs run on CUDA cores and attention on mma.sync tensor cores.
+ * The workspace of medusa_workspace_size covers it. Enqueues a 8-byte memset of
+ * the workspace (the barrier's count) and the kernel. No counterpart on the
+ * pages as an interface. */
+#define MEDUSA_FUSED_WAIT_CODE 0x40000000u
+MEDUSA_API int medusa_step_fused(const medusa_cfg* cfg, const medusa_step_args* args, medusa_stream_t stream);
+
 /* Tree attention over a paged KV cache. A page pool is read as a storage
  * layout of the same logical cache that medusa_tree_attention takes.
  *   Kp, Vp [num_pages][Hkv][page_rows][D] bf16  page pool of the committed rows

@@ -25,7 +25,7 @@ ENTRY_POINTS = ("medusa_node_count", "medusa_workspace_size", "medusa_heads", "m
                 "medusa_tree_attention", "medusa_verify", "medusa_kv_compact", "medusa_tree_attention_noalloc",
                 "medusa_tree_attention_paged", "medusa_kv_commit_paged", "medusa_step_graph_create",
                 "medusa_step_graph_launch", "medusa_step_graph_destroy", "medusa_poll_errors",
-                "medusa_selftest_wait_timeout", "medusa_checked_build", "medusa_poll_checks",
+                "medusa_selftest_wait_timeout", "medusa_checked_build", "medusa_poll_checks", "medusa_step_fused",
                 "medusa_launch_count", "medusa_status_string")
 CHECK_TOKEN, CHECK_TREE, CHECK_PATH, CHECK_PAGE = 1, 2, 4, 8
 
@@ -109,6 +109,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "medusa_step_graph_destroy": [P],
         "medusa_selftest_wait_timeout": [ctypes.c_uint32, P],
         "medusa_checked_build": [],
+        "medusa_step_fused": [cp, ctypes.POINTER(StepArgs), P],
         "medusa_poll_checks": [P, ctypes.POINTER(ctypes.c_uint32)],
     }
     for name, args in sig.items():
@@ -176,7 +177,19 @@ class StepGraph:
             pass
 
 
+def step_args(**buffers) -> "StepArgs":
+    """A medusa_step_args from tensors (None: NULL); kv_compact defaults to 1."""
+    return StepArgs(**{k: _ptr(v) for k, v in buffers.items() if k != "kv_compact"},
+                    kv_compact=int(bool(buffers.get("kv_compact", 1))))
+
+
+def step_fused(cfg: "Cfg", args: "StepArgs", stream=None) -> None:
+    """medusa_step_fused: the whole step as one persistent kernel launch."""
+    _check("medusa_step_fused", load().medusa_step_fused(ctypes.byref(cfg), ctypes.byref(args), _stream(stream)))
+
+
 WAIT_SELFTEST_CODE = 0x80000000
+FUSED_WAIT_CODE = 0x40000000
 STATUS_TIMEOUT = -5
 
 

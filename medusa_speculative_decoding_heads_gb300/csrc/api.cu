@@ -87,6 +87,8 @@ int medusa_workspace_size(const medusa_cfg* cfg, size_t* bytes) {
   if (s != MEDUSA_OK) return s;
   if (!bytes) return MEDUSA_ERR_INVALID_ARG;
   *bytes = align_up(heads_workspace(*cfg), 256) + align_up(attention_workspace(*cfg), 256) + verify_workspace(*cfg);
+  const size_t fused = fused_workspace(*cfg);   // the persistent step's own layout of the same buffer
+  if (fused > *bytes) *bytes = fused;
   return MEDUSA_OK;
 }
 
@@ -279,14 +281,32 @@ int medusa_step_graph_destroy(medusa_step_graph* g) {
 
 int medusa_poll_errors(medusa_stream_t stream, uint32_t* heads_codes, uint32_t* attention_codes) {
   cudaStream_t st = (cudaStream_t)stream;
-  uint32_t h = 0, a = 0;
+  uint32_t h = 0, a = 0, f = 0;
   cudaError_t e = heads_tc_take_error(&h, st);
   if (e == cudaSuccess) e = attention_tc_take_error(&a, st);
+  if (e == cudaSuccess) e = fused_take_error(&f, st);
+  a |= f;
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return MEDUSA_ERR_CUDA;
   if (heads_codes) *heads_codes = h;
   if (attention_codes) *attention_codes = a;
   return (h | a) ? MEDUSA_ERR_TIMEOUT : MEDUSA_OK;
+}
+
+int medusa_step_fused(const medusa_cfg* cfg, const medusa_step_args* a, medusa_stream_t stream) {
+  if (!cfg || !a) return MEDUSA_ERR_INVALID_ARG;
+  int s = check_cfg(cfg);
+  if (s != MEDUSA_OK) return s;
+  if (!fused_supported(*cfg)) return MEDUSA_ERR_UNSUPPORTED;
+  if (!a->h || !a->W || !a->U || !a->topk || !a->root_token || !a->L || !a->parent || !a->depth ||
+      !a->first_child || !a->mask || !a->anc_bits || !a->tokens || !a->pos || !a->Q || !a->Kc || !a->Vc || !a->O ||
+      !a->target_logits || !a->acc || !a->path || !a->out_tokens || !a->n_out || (a->kv_compact && !a->kv_map) ||
+      !a->workspace)
+    return MEDUSA_ERR_INVALID_ARG;
+  if (!aligned16(a->h) || !aligned16(a->W) || !aligned16(a->U) || (a->bias && !aligned16(a->bias)) ||
+      !aligned16(a->Q) || !aligned16(a->Kc) || !aligned16(a->Vc) || !aligned16(a->O) || !aligned16(a->target_logits))
+    return MEDUSA_ERR_INVALID_ARG;
+  return from_cuda(launch_fused_step(*cfg, *a, (cudaStream_t)stream));
 }
 
 int medusa_checked_build(void) {

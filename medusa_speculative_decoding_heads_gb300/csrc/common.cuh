@@ -169,6 +169,13 @@ cudaError_t launch_kv_compact(const medusa_cfg& c, void* Kc, void* Vc, int32_t* 
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The whole step as one persistent cooperative launch (fused.cu): small batches,
+// bf16, D = 128, greedy acceptance.
+bool fused_supported(const medusa_cfg& c);
+size_t fused_workspace(const medusa_cfg& c);
+cudaError_t launch_fused_step(const medusa_cfg& c, const medusa_step_args& s, cudaStream_t st);
+cudaError_t fused_take_error(uint32_t* out, cudaStream_t st);
+
 // Checked build (-DMEDUSA_CHECKED). Where a kernel meets an index it read from
 // device memory (a token id, a tree link, a path node, a page id) outside the
 // range it may address, it already clamps the index or skips the access; the

@@ -90,6 +90,24 @@ class DeviceStep:
             self.kv_compact(inp.Kc, inp.Vc, inp.L)
 
 
+    def fused_args(self, inp: "DeviceInputs", write_logits: bool = False, compact: bool = True) -> mb.StepArgs:
+        """The buffers of the five calls for medusa_step_fused (greedy; no uniforms)."""
+        if self.O is None or self.O.shape != inp.Q.shape:
+            self.O = torch.empty_like(inp.Q)
+        return mb.step_args(
+            h=inp.h, W=inp.W, bias=inp.bias, U=inp.U, logits=self.logits if write_logits else None, topk=self.topk,
+            root_token=inp.root_token, L=inp.L, parent=self.parent, depth=self.depth, first_child=self.first_child,
+            mask=self.mask, anc_bits=self.anc_bits, tokens=self.tokens, pos=self.pos, flags=self.flags, Q=inp.Q,
+            Kc=inp.Kc, Vc=inp.Vc, O=self.O, target_logits=inp.target_logits, u_acc=None, u_res=None, acc=self.acc,
+            path=self.path, out_tokens=self.out_tokens, n_out=self.n_out, kv_map=self.kv_map,
+            workspace=self.workspace, kv_compact=compact)
+
+    def run_fused(self, inp: "DeviceInputs", write_logits: bool = False, compact: bool = True):
+        """The whole step as one persistent kernel (medusa_step_fused)."""
+        args = self.fused_args(inp, write_logits, compact)
+        mb.step_fused(self.cfg, args, self.stream)
+        return args
+
     def graph(self, inp: "DeviceInputs", write_logits: bool = False, compact: bool = True) -> mb.StepGraph:
         """The same five calls captured once as a CUDA graph over these buffers (one launch per step)."""
         rs = self.mode == REJECTION

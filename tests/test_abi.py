@@ -160,3 +160,19 @@ def test_missing_library_fails_loudly(tmp_path):
             % (ROOT, str(tmp_path / "libmedusa.so")))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
     assert r.returncode == 3 and "not built" in r.stdout, (r.stdout, r.stderr)
+
+
+def test_step_fused_argument_checks():
+    """medusa_step_fused returns INVALID_ARG for missing arguments and UNSUPPORTED outside its
+    scope (float32, rejection sampling, B > 4) before any CUDA call."""
+    import ctypes
+    lib = mb.load()
+    c = mb.make_cfg(B=1, d=256, V=500, branching=(2, 2), Hq=2, Hkv=2, D=128, L_cap=256, dtype=mb.BF16,
+                    mode=mb.GREEDY)
+    assert lib.medusa_step_fused(ctypes.byref(c), None, None) == -1
+    args = mb.StepArgs()
+    for kw in (dict(dtype=mb.F32), dict(mode=mb.REJECTION), dict(B=5)):
+        cc = mb.make_cfg(**dict(dict(B=1, d=256, V=500, branching=(2, 2), Hq=2, Hkv=2, D=128, L_cap=256,
+                                     dtype=mb.BF16, mode=mb.GREEDY), **kw))
+        assert lib.medusa_step_fused(ctypes.byref(cc), ctypes.byref(args), None) == -2
+    assert lib.medusa_step_fused(ctypes.byref(c), ctypes.byref(args), None) == -1   # null buffers
