@@ -245,16 +245,18 @@ def test_attention_edge_lengths(L0, D):
     check_attention(w, si, st.O, [(b, kv) for b in range(w.B) for kv in range(w.Hkv)])
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("Hq,Hkv,branching", [(32, 16, (4, 3, 2, 1)), (40, 8, (4, 3, 2, 1)), (64, 8, (4, 3, 2, 1)),
                                               (32, 8, (2, 2, 2)), (32, 8, (6, 4, 4))])
-def test_attention_gqa_groups(Hq, Hkv, branching):
+def test_attention_gqa_groups(Hq, Hkv, branching, D):
     """Query-row tiles of 128 over N nodes x G heads: G = 2, 5, 8 with the 65-node tree
     (2, 3, 5 tiles per KV head, ragged last tiles), a 15-node tree (one partial tile) and a
-    127-node tree (two mask words per node, 4 tiles); single and split KV ranges (B = 1 and 6)."""
+    127-node tree (two mask words per node, 4 tiles); single and split KV ranges (B = 1 and 6);
+    head dims 128 (tcgen05) and 64 (mma.sync)."""
     dev = gpu_ready()
     for B, L_range in ((1, (700, 700)), (6, (0, 900))):
         w = configs.scaled(configs.get("gqa7b_b32"), B=B, d=64, V=64, Hq=Hq, Hkv=Hkv, branching=branching,
-                           L_range=L_range)
+                           L_range=L_range, D=D)
         si = synth.make_step_inputs(w, seed=Hq + Hkv + B, device=dev)
         st = run_attention(w, si, dev)
         check_attention(w, si, st.O, [(b, kv) for b in range(w.B) for kv in (0, Hkv // 2, Hkv - 1)])
