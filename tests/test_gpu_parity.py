@@ -245,6 +245,19 @@ def test_attention_edge_lengths(L0, D):
     check_attention(w, si, st.O, [(b, kv) for b in range(w.B) for kv in range(w.Hkv)])
 
 
+@pytest.mark.parametrize("G", [1, 5])
+@pytest.mark.parametrize("L0", [0, 1, 127, 128, 129])
+def test_attention_edge_lengths_without_leftover_rows(L0, G):
+    """The tcgen05 kernel without leftover rows (G = 1: one 65-row Q tile; G = 5: 325 rows in
+    Q tiles of 128, 128 and 69 rows) at the prefix lengths around a key tile: no prefix, a
+    one-key prefix tile ahead of the tree tile, one and two full tiles."""
+    dev = gpu_ready()
+    w = configs.scaled(configs.get("gqa7b_b32"), B=2, d=64, V=64, L_range=(L0, L0), Hq=2 * G, Hkv=2)
+    si = synth.make_step_inputs(w, seed=L0 + G, device=dev)
+    st = run_attention(w, si, dev)
+    check_attention(w, si, st.O, [(b, kv) for b in range(w.B) for kv in range(w.Hkv)])
+
+
 @pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("Hq,Hkv,branching", [(32, 16, (4, 3, 2, 1)), (40, 8, (4, 3, 2, 1)), (64, 8, (4, 3, 2, 1)),
                                               (32, 8, (2, 2, 2)), (32, 8, (6, 4, 4))])
