@@ -50,7 +50,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one call of the step's dominant call, from full-size ncu captures
 # of its kernels (one pass each; summarised in profiles/). Absent = not captured: traffic null.
 NCU_TRAFFIC_BYTES = {"vicuna7b_b1": 1189250048, "vicuna7b_b1_shared": 402850048, "vicuna13b_b8": 1918169600}   # medusa_heads
-NCU_ATTN_TRAFFIC_BYTES = {"gqa7b_b32": 1512026112, "vicuna33b_b16": 3573742592}   # medusa_tree_attention
+NCU_ATTN_TRAFFIC_BYTES = {"gqa7b_b32": 1512010496, "vicuna33b_b16": 3573742592}   # medusa_tree_attention
 
 
 def parse():

@@ -179,8 +179,10 @@ __device__ __forceinline__ float exp32(const uint32_t* v, float scale_log2, floa
   return a.x + a.y;
 }
 
-template <bool kFold>
-__global__ void __launch_bounds__(threads_of(kFold), 1)
+// kXR: 0 without leftover rows, else the number of leftover rows rounded up to 2, 4 or 8
+// (the leftover softmax's per-row loops run to kXR).
+template <int kXR>
+__global__ void __launch_bounds__(threads_of(kXR > 0), 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt,
                     const uint16_t* __restrict__ Q, const int32_t* __restrict__ L, const uint64_t* __restrict__ bits,
@@ -226,6 +228,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   // (tiles j with j % MT == mt), so that the CTAs that share each K/V tile through L2 keep the
   // same pace; their partial results merge in tree_attn_xmerge_kernel.
   const int MT = (int)gridDim.x;
+  constexpr bool kFold = kXR > 0;
   const int R = kFold ? extra_rows(NG) : 0;
   const bool xtra = R > 0;
   const bool xs = xtra && warp >= kXWarp0 && warp < kXWarp0 + 4;   // a leftover-row softmax thread
@@ -646,21 +649,20 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       tc::tmem_wait_ld();
       const bool tree = j >= ptiles;
       const int nkeys = tree ? N : min(kKeys, k_end - (k_begin + j * kKeys));
-      float x[kXMax];
+      float x[kXR > 0 ? kXR : 1];
 #pragma unroll
-      for (int r = 0; r < kXMax; ++r) {
+      for (int r = 0; r < kXR; ++r) {
         bool vis = r < R && xt < nkeys;
         if (vis && tree) vis = (bits[2 * ((xq0 + r) / G) + (xt >> 6)] >> (xt & 63)) & 1ull;
         x[r] = vis ? __uint_as_float(v[r]) * scale_log2 : -INFINITY;
       }
-      float* rm = red + 64 * slot;
+      float* rm = red + 64 * slot;   // tile maxima [row][warp]
 #pragma unroll
-      for (int r = 0; r < kXMax; ++r) {
+      for (int r = 0; r < kXR; ++r) {
         if (r < R) {
-          float m = x[r];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          if (lane == 0) rm[16 * (warp & 3) + r] = m;
+          float m;
+          asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(x[r]));
+          if (lane == 0) rm[4 * r + (warp & 3)] = m;
         }
       }
       tc::mbar_arrive(&xbar2);
@@ -671,10 +673,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       }
       bool any = false;
 #pragma unroll
-      for (int r = 0; r < kXMax; ++r) {
+      for (int r = 0; r < kXR; ++r) {
         corr[r] = 1.f;
         if (r < R) {
-          const float m_tile = fmaxf(fmaxf(rm[r], rm[16 + r]), fmaxf(rm[32 + r], rm[48 + r]));
+          const float4 mw = *reinterpret_cast<const float4*>(rm + 4 * r);
+          const float m_tile = fmaxf(fmaxf(mw.x, mw.y), fmaxf(mw.z, mw.w));
           if (m_tile > m_run[r] + kLazy) {   // also on the first tile (m_run = -inf): corr = 0
             corr[r] = tc::ex2(m_run[r] - m_tile);
             m_run[r] = m_tile;
@@ -687,7 +690,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       uint8_t* pr = sm + kOffPx + slot * 2 * kXHalf + (xt >> 6) * kXHalf;
       const int cc = xt & 63;
 #pragma unroll
-      for (int r = 0; r < kXMax; ++r) {
+      for (int r = 0; r < kXR; ++r) {
         if (r < R) {
           const float pv = x[r] == -INFINITY ? 0.f : tc::ex2(x[r] - m_run[r]);
           l_t[r] = l_t[r] * corr[r] + pv;
@@ -708,7 +711,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         tc::tmem_ld8(tmem + kColO2 + xl_base, ov);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int r = 0; r < kXMax; ++r) ov[r] = __float_as_uint(__uint_as_float(ov[r]) * corr[r]);
+        for (int r = 0; r < kXR; ++r) ov[r] = __float_as_uint(__uint_as_float(ov[r]) * corr[r]);
         tc::tmem_st8(tmem + kColO2 + xl_base, ov);
       }
       tc::fence_proxy_async();   // the P' stores, visible to the tensor core
@@ -907,7 +910,9 @@ cudaError_t launch_attention_tc(const medusa_cfg& c, int nsplit, int chunk, cons
   const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)kD));
   const int NG = ts.N * (c.Hq / c.Hkv);
   const bool fold = extra_rows(NG) > 0;
-  auto kernel = fold ? tree_attn_tc_kernel<true> : tree_attn_tc_kernel<false>;
+  const int R = extra_rows(NG);
+  auto kernel = !fold ? tree_attn_tc_kernel<0>
+                      : R <= 2 ? tree_attn_tc_kernel<2> : R <= 4 ? tree_attn_tc_kernel<4> : tree_attn_tc_kernel<8>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_of(fold));
   if (e != cudaSuccess) return e;
   dim3 grid(attention_tc_mtiles(NG), c.Hkv * c.B, nsplit);
