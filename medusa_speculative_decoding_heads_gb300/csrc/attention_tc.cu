@@ -32,9 +32,13 @@
 //           narrow products on those K/V tiles: S'^T = K Q'^T (M = 128 keys,
 //           N = 16 rows) right behind S_j, and O'^T += V^T P'^T (M = 128 head
 //           dims) right behind PV_j, whose completion then frees the stage. Q'
-//           and P' sit in shared memory. Thread = key (S') or head dim (O'); row
-//           maxima cross the four warps through shared memory. Each CTA writes
-//           its partial (O', m, l); tree_attn_xmerge_kernel merges them.
+//           and P' sit in shared memory. Thread = key (S') or head dim (O'); a
+//           row's maximum over a warp's 32 keys is one redux.sync, and the four
+//           warps' maxima meet in shared memory. The per-row loops run to the
+//           leftover row count rounded up to 2, 4 or 8 (the kernel's template
+//           argument): these warps share the SM sub-partitions' issue slots with
+//           the softmax warps. Each CTA writes its partial (O', m, l);
+//           tree_attn_xmerge_kernel merges them.
 // Every mbarrier wait is bounded (a few seconds of clock cycles); on expiry the
 // thread records a code in a device error word and leaves its loop.
 #include <cuda.h>
