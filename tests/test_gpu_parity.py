@@ -245,6 +245,37 @@ def test_attention_edge_lengths(L0, D):
     check_attention(w, si, st.O, [(b, kv) for b in range(w.B) for kv in range(w.Hkv)])
 
 
+@pytest.mark.parametrize("name,D", [("tiny_fp32", None), ("vicuna7b_b1", 128), ("gqa7b_b32", 128),
+                                    ("gqa7b_b32", 64)])
+@pytest.mark.parametrize("Lmax", [100, 900])
+def test_attention_invalid_sequences_get_zeros(name, D, Lmax):
+    """A sequence with L_b < 0 or L_b + N > L_cap gets O = 0 (the header's contract), on every
+    attention kernel (float32, tcgen05 with and without leftover rows, mma.sync at D = 64) with
+    one KV range and with several; the valid sequences still match the oracle."""
+    dev = gpu_ready()
+    base = configs.get(name)
+    G = base.Hq // base.Hkv
+    kw = dict(B=4, d=64, V=64, Hq=2 * G, Hkv=2, L_range=(Lmax // 2, Lmax))
+    if D is not None:
+        kw["D"] = D
+    w = configs.scaled(base, **kw)
+    si = synth.make_step_inputs(w, seed=Lmax + (D or 0), device=dev)
+    L = si.L.copy()
+    L[1] = si.L_cap - w.N + 1   # one row past the capacity
+    L[2] = -1
+    st = DeviceStep(w, w.modes[0], si.L_cap, dev)
+    Ld = torch.from_numpy(L).to(dev)
+    st.tree_build(torch.from_numpy(si.root_token).to(dev), Ld,
+                  topk=torch.zeros((w.B, w.K, w.s_max), dtype=torch.int32, device=dev))
+    st.O = torch.full_like(si.Q, float("nan"))
+    st.tree_attention(si.Q, si.Kc, si.Vc, Ld)
+    torch.cuda.synchronize()
+    O_gpu = st.O.cpu()
+    assert torch.count_nonzero(O_gpu[1:3]).item() == 0, "invalid sequences must get O = 0"
+    si.L = L
+    check_attention(w, si, O_gpu, [(b, kv) for b in (0, 3) for kv in range(w.Hkv)])
+
+
 @pytest.mark.parametrize("G", [1, 5])
 @pytest.mark.parametrize("L0", [0, 1, 127, 128, 129])
 def test_attention_edge_lengths_without_leftover_rows(L0, G):
