@@ -494,6 +494,46 @@ def test_kv_compact_bit_exact(name):
     assert np.array_equal(i64(Ld), Lr) and np.array_equal(i64(st.kv_map), kv_map)
 
 
+@pytest.mark.parametrize("name", ["tiny_fp32", "vicuna33b_b16", "gqa7b_b32"])
+def test_kv_compact_leaves_invalid_sequences(name):
+    """Sequences with L_b < 0 or L_b + N > L_cap are left unchanged (the header's contract):
+    cache rows and length bit-exact, kv_map -1; the other sequences match the oracle."""
+    dev = gpu_ready()
+    base = configs.get(name)
+    hkv = 2 if base.Hkv < 8 else 8               # 8 KV heads: the compaction cluster's full width
+    w = configs.scaled(base, B=5, d=64, V=64, Hq=hkv * (base.Hq // base.Hkv), Hkv=hkv, L_range=(20, 300))
+    si = synth.make_step_inputs(w, seed=41, device=dev)
+    rng = np.random.default_rng(41)
+    tree = layout(w)
+    acc, path = random_paths(tree, w.K, w.B, rng)
+    acc[1], acc[3] = w.K, w.K                    # full paths on the two invalid sequences
+    for b in (1, 3):
+        cur, path[b, 0] = 0, 0
+        for r in range(1, w.K + 1):
+            kids = O.children_of(tree["parent"], cur)
+            cur = kids[-1]
+            path[b, r] = cur
+    L = si.L.copy()
+    L[1] = si.L_cap - w.N + 1   # over capacity
+    L[3] = -1
+    raw = lambda t: t.cpu().view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32).numpy()
+    k0, v0 = raw(si.Kc), raw(si.Vc)
+    st = DeviceStep(w, w.modes[0], si.L_cap, dev)
+    st.acc.copy_(torch.from_numpy(acc))
+    st.path.copy_(torch.from_numpy(path))
+    Ld = torch.from_numpy(L).to(dev)
+    st.kv_compact(si.Kc, si.Vc, Ld)
+    torch.cuda.synchronize()
+    k1, v1, L1, kv_map = raw(si.Kc), raw(si.Vc), i64(Ld), i64(st.kv_map)
+    for b in (1, 3):
+        assert np.array_equal(k1[b], k0[b]) and np.array_equal(v1[b], v0[b]), f"sequence {b} changed"
+        assert L1[b] == L[b] and (kv_map[b] == -1).all()
+    ok = np.array([0, 2, 4])
+    kr, vr, Lr, mr = O.kv_compact(k0[ok], v0[ok], L[ok], acc[ok], path[ok])
+    assert np.array_equal(k1[ok], kr) and np.array_equal(v1[ok], vr)
+    assert np.array_equal(L1[ok], Lr) and np.array_equal(kv_map[ok], mr)
+
+
 def random_paths(tree, K, B, rng):
     """acc uniform in 0..K with sequence 0 at acc = 0 and the last at acc = K; a random descent."""
     acc = rng.integers(0, K + 1, size=B).astype(np.int32)
