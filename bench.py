@@ -502,6 +502,8 @@ def run_ours(args):
     ms_per_step = elapsed_ms / args.steps
 
     e2e = None if args.no_e2e else run_e2e(w, st, inp, L0, tl, si, args, stream, world)
+    # every bounded device wait of the run completed (a wait that expired would have cut its work short)
+    wait_status, heads_codes, attention_codes = mb.poll_errors()
 
     if rank != 0:
         if world > 1:
@@ -542,12 +544,17 @@ def run_ours(args):
         "launch_mode": launch_mode + (", medusa_step_fused" if args.fused else ""),
         "accepted_per_step": float(np.mean(acc + 1)),
         "e2e": e2e,
+        "expired_waits": {"status": wait_status, "heads": heads_codes, "attention": attention_codes},
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, mode, si, tl)
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+    if wait_status != 0:
+        print(f"# a bounded device wait expired during the run (heads {heads_codes:#x}, attention "
+              f"{attention_codes:#x}): the numbers above are not valid", file=sys.stderr)
+        return 3
     return 0
 
 
