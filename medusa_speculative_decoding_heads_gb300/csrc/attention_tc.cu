@@ -627,11 +627,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   } else if (xs) {
     // ------------------------------------------------------- leftover-row softmax
     // Thread xt holds key xt of S'^T (one score per leftover row) and head dim xt of
-    // O'^T. This CTA's narrow tiles are the key tiles j = jx * MT + mt. Row maxima: warp
-    // shuffles, then the four warps' values through shared memory (double-buffered by
-    // the narrow tile's parity, one mbarrier phase per narrow tile).
+    // O'^T. This CTA's narrow tiles are the key tiles j = jx * MT + mt. Row maxima: one
+    // redux.sync per row and warp, then the four warps' values through shared memory
+    // (double-buffered by the narrow tile's parity, one mbarrier phase per narrow tile).
     const uint32_t xl_base = (uint32_t)(32 * (warp & 3)) << 16;
-    float* red = reinterpret_cast<float*>(sm + kOffRed);   // maxima [parity][warp][row], then sums [warp][row]
+    float* red = reinterpret_cast<float*>(sm + kOffRed);   // maxima [parity][row][warp], then sums [warp][row]
     const int nx = ntiles > mt ? (ntiles - 1 - mt) / MT + 1 : 0;
     float m_run[kXMax], l_t[kXMax], corr[kXMax];
 #pragma unroll
