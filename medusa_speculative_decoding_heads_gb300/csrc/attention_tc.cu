@@ -193,7 +193,6 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     int N, int Hq, int Hkv, int L_cap, int chunk, float scale_log2, float* __restrict__ o_part,
                     float* __restrict__ ml_part, uint16_t* __restrict__ O, const int32_t* __restrict__ block_table,
                     int page_rows, int num_pages, float* __restrict__ x_part) {
-  pdl_wait();
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -205,6 +204,37 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   __shared__ uint32_t tmem_slot;
   __shared__ int seq;
   uint32_t* err = &g_attention_tc_error;
+
+  // Barriers and TMEM are set up before the wait on the previous kernel (neither touches
+  // global memory), so that this overlaps its tail.
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStagesK; ++i) {
+      tc::mbar_init(&k_full[i], 1);
+      tc::mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < kStagesV; ++i) {
+      tc::mbar_init(&v_full[i], 1);
+      tc::mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&s_full[i], 1);
+      tc::mbar_init(&p_full[i], kSoftmaxWarps * 32);
+      tc::mbar_init(&p_free[i], 1);
+    }
+    tc::mbar_init(&xbar, kSoftmaxWarps * 32);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&s2_full[i], 1);
+      tc::mbar_init(&p2_full[i], 128);
+      tc::mbar_init(&p2_free[i], 1);
+    }
+    tc::mbar_init(&xbar2, 128);
+    tc::mbar_fence_init();
+  }
+  if ((threadIdx.x >> 5) == kProducerWarp) tc::tmem_alloc(&tmem_slot, kTmemCols);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  pdl_wait();   // the previous kernel's writes (L, the cache) are visible from here on
 
   // Launch order: x = Q tile (fastest, so the tiles of one KV head share its K/V
   // through L2), y = (sequence rank, KV head), z = KV split. Sequences are taken
@@ -282,36 +312,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           ml_part[2 * orow + 1] = 0.f;
         }
       }
+    if (warp == kProducerWarp) tc::tmem_dealloc(tmem_slot, kTmemCols);
     return;
   }
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kStagesK; ++i) {
-      tc::mbar_init(&k_full[i], 1);
-      tc::mbar_init(&k_empty[i], 1);
-    }
-    for (int i = 0; i < kStagesV; ++i) {
-      tc::mbar_init(&v_full[i], 1);
-      tc::mbar_init(&v_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&s_full[i], 1);
-      tc::mbar_init(&p_full[i], kSoftmaxWarps * 32);
-      tc::mbar_init(&p_free[i], 1);
-    }
-    tc::mbar_init(&xbar, kSoftmaxWarps * 32);
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&s2_full[i], 1);
-      tc::mbar_init(&p2_full[i], 128);
-      tc::mbar_init(&p2_free[i], 1);
-    }
-    tc::mbar_init(&xbar2, 128);
-    tc::mbar_fence_init();
-  }
-  if (warp == kProducerWarp) tc::tmem_alloc(&tmem_slot, kTmemCols);
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
   const uint32_t tmem = tmem_slot;
   const uint32_t tQ = tmem + kColQ;
 
