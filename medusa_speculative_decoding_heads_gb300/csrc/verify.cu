@@ -740,7 +740,6 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
                const T* __restrict__ tl, const float* __restrict__ hl,
                const float2* __restrict__ hstats, int hsP, const float* __restrict__ u_acc,
                const float* __restrict__ u_res, WalkOut w) {
-  pdl_wait();
   pdl_trigger();
   extern __shared__ float buf[];   // inverse-CDF transpose, [C][kPad]
   __shared__ Scratch<kVWarps> s;
@@ -751,6 +750,16 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
   const int b = blockIdx.x / ncta, N = ts.N, K = ts.K;
   const int lo = min(V, (int)rank * slice), hi = min(V, lo + slice);
   const float c = 1.4426950408889634f / Tmp;
+  // the exchange barriers and the cluster barrier touch no global memory, so they are set
+  // up before the wait on the previous kernel and overlap its tail
+  if (threadIdx.x == 0) {
+    tc_free_mbar_init(&x.bar[0], ncta);
+    tc_free_mbar_init(&x.bar[1], ncta);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    path[0] = 0;
+  }
+  cluster_sync();   // every CTA's barriers exist before any peer arrives on them
+  pdl_wait();
   // this sequence's tree tokens and the tree's first-child table, staged once
   __shared__ int s_tok[kMaxN], s_fc[kMaxN], s_par[kMaxN];
   for (int i = threadIdx.x; i < N; i += kVThreads) {
@@ -761,13 +770,6 @@ rs_walk_kernel(TreeShape ts, int V, int slice, float Tmp, const int32_t* __restr
   }
   uint32_t fl = 0;
   int xn = 0;
-  if (threadIdx.x == 0) {
-    tc_free_mbar_init(&x.bar[0], ncta);
-    tc_free_mbar_init(&x.bar[1], ncta);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    path[0] = 0;
-  }
-  cluster_sync();   // every CTA's barriers exist before any peer arrives on them
   // the candidates of the current depth: token, its target and head logits, and
   // the acceptance uniform, fetched before the row sweep so that their load
   // latency overlaps it
